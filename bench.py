@@ -1,0 +1,422 @@
+"""Benchmark of batched paged-KV GQA decode on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step is one batched paged-decode call (decode kernel + merge kernel; for
+the append workload, an append then a decode) over the workload's batch,
+inputs resident in HBM. L2 is flushed between timed steps, outside the timed
+events. Prints one JSON line: achieved HBM TB/s = (K+V+q+o bytes) / device
+time per call, with the roofline of the decode kernel, the CPU oracle timed on
+the host as a reported baseline, an end-to-end figure through the C ABI with
+host buffers, and SM clocks sampled during the run.
+
+--impl reference times the CPU oracle (the reference arm: there is no
+runnable reference implementation) on a bounded sample of the same workload.
+Under torchrun every rank runs its own replica on its own GPU (the decode has
+no exchange step); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM TB/s (% of GB300 peak) and us per batched paged-decode call"
+UNIT = "TB/s"
+DEFAULT_CONFIG = "llama3_8b"
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["paged_kv_gqa_13_gb300/csrc/pd_decode.cuh", "paged_kv_gqa_13_gb300/csrc/pd_device.cuh"]
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_sha()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[2] == sha:
+                return int(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle samples while the benchmark runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.marks = {}
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0, t1 = self.marks.get("timed_start", 0), self.marks.get("timed_end", 1e30)
+        timed = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not timed:
+            timed = [p for (_, p) in self.samples]
+            window = "whole run (timed region shorter than the 100 ms sampling period)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in timed if num(p[1]) is not None]
+        mx = [num(p[2]) for p in timed if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in timed for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(timed), "window": window}
+
+
+# ---------------------------------------------------------------- workloads
+
+def load_workload(name: str, rank: int = 0):
+    import workloads as wl
+
+    if name == "long_context_contiguous":
+        return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous"
+    return wl.CONFIGS[name](seed=wl.CONFIGS[name].__defaults__[0] + 100 * rank), "paged"
+
+
+def algorithmic_bytes(w, table=None) -> int:
+    return w.kv_bytes(table) + w.qo_bytes()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+    import workloads as wl
+
+    def to_dev(raw, dtype, device):
+        if dtype == "f32":
+            return torch.from_numpy(np.ascontiguousarray(raw)).to(device)
+        t = torch.from_numpy(np.ascontiguousarray(raw).view(np.int16)).to(device)
+        return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
+
+    def table_dev(t, device):
+        return tuple(torch.from_numpy(x.astype(np.int32)).to(device)
+                     for x in (t.indices, t.indptr, t.last_page_len))
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w, mode = load_workload(args.config, rank)
+    code = {"f32": pd.PD_F32, "f16": pd.PD_F16, "bf16": pd.PD_BF16}[w.dtype]
+    stream = torch.cuda.current_stream()
+
+    q = to_dev(w.q, w.dtype, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device=dev)
+    tables = [w.table]
+    appends = []
+    if mode == "contiguous":
+        kc, vc, n_valid = wl.contiguous_copy(w)
+        k = to_dev(kc, w.dtype, dev)
+        v = to_dev(vc, w.dtype, dev)
+        del kc, vc
+        ws = pd.alloc_workspace(pd.pd_contiguous_decode_workspace_bytes(
+            w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, code), dev)
+
+        def step(i):
+            pd.pd_contiguous_decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
+        bytes_per_step = [algorithmic_bytes(w)]
+    else:
+        k = to_dev(w.k_data, w.dtype, dev)
+        v = to_dev(w.v_data, w.dtype, dev)
+        ws = pd.alloc_workspace(pd.pd_paged_decode_workspace_bytes(
+            w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, code), dev)
+        if w.append_steps:
+            # append-then-decode: each step appends one row per request, then decodes
+            t = w.table
+            for s in range(w.append_steps):
+                t = wl.table_after_append(t)
+                tables.append(t)
+                kn, vn = w.new_rows(s)
+                appends.append((to_dev(kn, w.dtype, dev), to_dev(vn, w.dtype, dev)))
+            tables = tables[1:]
+        dev_tables = [table_dev(t, dev) for t in tables]
+
+        # Step i uses table i mod steps. Repeating the sequence rewrites the same
+        # rows with the same bytes, and a decode never reads rows appended later,
+        # so the cache needs no reset between repetitions.
+        def step(i):
+            if w.append_steps:
+                j = i % w.append_steps
+                ind, ptr, lpl = dev_tables[j]
+                kn, vn = appends[j]
+                pd.pd_paged_append(kn, vn, k, v, ind, ptr, lpl, ws)
+            else:
+                ind, ptr, lpl = dev_tables[0]
+            pd.pd_paged_decode(q, k, v, ind, ptr, lpl, o, lse, w.sm_scale, ws)
+        bytes_per_step = [algorithmic_bytes(w, t) for t in tables]
+        if w.append_steps:
+            ab = 2 * w.batch * w.num_kv_heads * w.head_dim * wl.ELEM_BYTES[w.dtype] * 2
+            bytes_per_step = [b + ab for b in bytes_per_step]
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # in-process copy-kernel bandwidth (reported beside the driver's measured peak)
+    src = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        pd.pd_copy_bytes(dst, src)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        pd.pd_copy_bytes(dst, src)
+    e1.record()
+    torch.cuda.synchronize()
+    copy_gbs = 2 * src.numel() * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del src, dst
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    entries = [x.strip() for x in visible.split(",") if x.strip()]
+    sampler = ClockSampler(entries[local_rank] if local_rank < len(entries) else local_rank)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    pd.pd_profile_read()  # discard anything recorded before
+    pd.pd_profile_enable(True)
+    sampler.mark("timed_start")
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # evict K/V of the previous step from L2 (outside the timed events)
+        starts[i].record(stream)
+        step(args.warmup + i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    sampler.mark("timed_end")
+    pd.pd_profile_enable(False)
+    prof = pd.pd_profile_read()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_mean = float(np.mean(ms))
+    byte_steps = [bytes_per_step[(args.warmup + i) % len(bytes_per_step)] for i in range(args.steps)]
+    bytes_mean = float(np.mean(byte_steps))
+
+    # end to end through the C ABI with host buffers: per step, copy q and the
+    # page table in from pinned host memory, decode, copy o and lse out.
+    e2e = None
+    if mode == "paged" and not w.append_steps:
+        t = tables[0]
+        hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16 if w.dtype != "f32" else np.float32)).pin_memory()
+        h_ind = torch.from_numpy(t.indices.astype(np.int32)).pin_memory()
+        h_ptr = torch.from_numpy(t.indptr.astype(np.int32)).pin_memory()
+        h_lpl = torch.from_numpy(t.last_page_len.astype(np.int32)).pin_memory()
+        h_o = torch.empty(o.numel() * o.element_size(), dtype=torch.uint8).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        d_ind, d_ptr, d_lpl = dev_tables[0]
+        q_raw = q.view(torch.int16) if w.dtype != "f32" else q
+        h2d = hq.numel() * hq.element_size() + 4 * (h_ind.numel() + h_ptr.numel() + h_lpl.numel())
+        d2h = h_o.numel() + 4 * h_lse.numel()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        for i in range(args.warmup + args.steps):
+            if i >= args.warmup:
+                flush.zero_()
+                es[2 * (i - args.warmup)].record(stream)
+            q_raw.copy_(hq, non_blocking=True)
+            d_ind.copy_(h_ind, non_blocking=True)
+            d_ptr.copy_(h_ptr, non_blocking=True)
+            d_lpl.copy_(h_lpl, non_blocking=True)
+            pd.pd_paged_decode(q, k, v, d_ind, d_ptr, d_lpl, o, lse, w.sm_scale, ws)
+            h_o.copy_(o.view(torch.uint8).view(-1), non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            if i >= args.warmup:
+                es[2 * (i - args.warmup) + 1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([es[2 * j].elapsed_time(es[2 * j + 1]) for j in range(args.steps)]))
+        e2e = {"value": bytes_mean / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    clocks = sampler.stop()
+    return {"w": w, "mode": mode, "ms_mean": ms_mean, "ms_all": ms, "bytes_mean": bytes_mean, "prof": prof,
+            "copy_gbs": copy_gbs, "e2e": e2e, "clocks": clocks, "t_wall": t_wall}
+
+
+def cpu_baseline(w, mode: str, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands, on all host cores, repeated on the full workload for ~budget_s."""
+    import oracle
+    import workloads as wl
+
+    threads = oracle.hardware_threads()
+    table = w.table
+    if w.append_steps:
+        table = wl.table_after_append(w.table)
+    if mode == "contiguous":
+        kc, vc, nv = wl.contiguous_copy(w)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        if mode == "contiguous":
+            oracle.contiguous_decode(w.q, kc, vc, w.num_qo_heads, nv, w.sm_scale, w.dtype, threads)
+        else:
+            oracle.paged_decode_workload(w, table=table, threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (n >= 1 and el * (n + 1) / n > 3 * budget_s):
+            break
+    per = el / n
+    value = algorithmic_bytes(w, table) / per / 1e12
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full {w.name} decode, {n} call(s), {per * 1e3:.1f} ms per call on {threads} threads"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=["tiny", "llama3_8b", "long_context", "long_context_contiguous", "ragged_70b",
+                             "mha_append"])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w, mode = load_workload(args.config)
+        for _ in range(args.warmup):
+            pass  # the oracle has no warm state; warm-up calls would only repeat the timing
+        cb = cpu_baseline(w, mode, budget_s=max(5.0, min(60.0, 2.0 * args.steps)))
+        per_ms = algorithmic_bytes(w) / (cb["value"] * 1e12) * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": {"workload": w.name}, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    r = run_gpu(args, rank, world, local_rank)
+    ms_max = r["ms_mean"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_max], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    w = r["w"]
+    tbps = world * r["bytes_mean"] / (ms_max * 1e-3) / 1e12
+    peaks = measured_peaks()
+    prof = r["prof"]
+    dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
+    dec_bytes = r["bytes_mean"]
+    achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
+    traffic = recorded_traffic("decode_kernel", w.name)
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
+                "peak_source": peaks["source"], "kernel": "decode_kernel",
+                "kernel_us": dec_ms * 1e3, "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
+                "copy_kernel_gbs": r["copy_gbs"]}
+    cb = None if args.no_cpu_baseline else cpu_baseline(w, r["mode"])
+    launches = prof["decode_launches"] + prof["merge_launches"] + (args.steps if w.append_steps else 0)
+    ms = r["ms_all"]
+    line = {
+        "metric": METRIC, "value": tbps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "mode": r["mode"], "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                   "kv_tokens": int(w.table.kv_len().sum()), "bytes_per_step": int(r["bytes_mean"]),
+                   "l2": "flushed (512 MB write) before every timed step, outside the timed events",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": ms_max * 1e3,
+        "us_p10_p50_p90": [float(np.percentile(ms, x)) * 1e3 for x in (10, 50, 90)],
+        "rows_per_s": world * w.batch / (ms_max * 1e-3),
+        "pct_of_peak": 100.0 * tbps * 1e3 / world / peaks["hbm_gbs"],
+        "roofline": roofline, "cpu_baseline": cb, "e2e": r["e2e"], "gpu_launches": launches,
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

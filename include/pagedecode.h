@@ -1,0 +1,220 @@
+/*
+ * pagedecode: batched single-query (decode-phase) grouped-query attention over
+ * a paged KV cache, for NVIDIA sm_103a (GB300).
+ *
+ * The problem statement followed here is the module documentation of
+ * baracuda-kernels 0.0.1-alpha.68, src/attention/batch_paged_decode.rs,
+ * sections "Layout" and "Constraints", and its descriptor and argument types
+ * (PagedKvCacheDescriptor, BatchPagedDecodeDescriptor, BatchPagedDecodeArgs):
+ *
+ *   k_data, v_data  [num_total_pages, num_kv_heads, page_size, head_dim]  T, HND
+ *   indices         [num_indices]  int32  physical page ids
+ *   indptr          [batch + 1]    int32  request b owns indices[indptr[b] .. indptr[b+1])
+ *   last_page_len   [batch]        int32  valid rows in request b's last page, 0..page_size
+ *   q, o            [batch, num_qo_heads, head_dim]  T
+ *   lse             [batch, num_qo_heads]  float32 (whatever T is)
+ *
+ * For request b with np = indptr[b+1] - indptr[b] pages, kv_len = (np - 1) *
+ * page_size + last_page_len[b] (0 when np = 0); token t is row t % page_size of
+ * page indices[indptr[b] + t / page_size]. Query head h reads kv head
+ * h / (num_qo_heads / num_kv_heads) (ferrox-cuda 0.15.2, src/attn.rs,
+ * gqa_decode). With s_t = sm_scale * q[b,h,:] . k_t:
+ *
+ *   o[b,h,:]  = sum_t exp(s_t - lse) * v_t        lse[b,h] = ln sum_t exp(s_t)
+ *
+ * An empty request (kv_len = 0) gets o = 0 and lse = -infinity.
+ *
+ * Conventions shared by every call:
+ *  - Pointers marked "device" are CUDA device pointers (or managed memory) on
+ *    the current device; host pointers are marked "host". The caller owns
+ *    every buffer, including the page table and its allocator; the library
+ *    allocates no memory on any call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream). No call blocks the host except the two marked "synchronizes".
+ *  - T is given by `dtype`: PD_F32 float, PD_F16 IEEE half, PD_BF16 bfloat16.
+ *    Accumulation is float32 for every T. Results are bit-identical across
+ *    repeated calls with the same arguments on the same device.
+ *  - Arguments are checked on the host before anything is enqueued; a failed
+ *    check returns an error status, enqueues nothing and sets the message
+ *    returned by pd_last_error_string(). Values that live in device memory
+ *    (page ids, indptr, last_page_len) are checked by the kernels: a bad
+ *    value sets a bit of the sticky status word in the workspace header (see
+ *    PD_FLAG_*), the offending page or request is treated as empty, and the
+ *    kernel carries on. No kernel traps.
+ *  - Status codes: PD_ERR_INVALID for malformed extents or null pointers,
+ *    PD_ERR_UNSUPPORTED for a head_dim, dtype or pointer alignment this
+ *    library does not handle, PD_ERR_WORKSPACE for a missing or small
+ *    workspace, PD_ERR_CUDA when the CUDA runtime reports an error.
+ */
+#ifndef PAGEDECODE_H
+#define PAGEDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PD_VERSION 1
+
+typedef enum { PD_F32 = 0, PD_F16 = 1, PD_BF16 = 2 } pd_dtype;
+
+typedef enum {
+    PD_OK = 0,
+    PD_ERR_INVALID = 1,
+    PD_ERR_UNSUPPORTED = 2,
+    PD_ERR_WORKSPACE = 3,
+    PD_ERR_CUDA = 4
+} pd_status;
+
+/* Bits of the sticky device status word (first int32 of every workspace). */
+#define PD_FLAG_BAD_PAGE_ID 0x1       /* a page id outside [0, num_total_pages): page treated as empty */
+#define PD_FLAG_BAD_LAST_PAGE_LEN 0x2 /* last_page_len outside [0, page_size]: clamped to that range */
+#define PD_FLAG_BAD_INDPTR 0x4        /* indptr decreasing, negative or past num_indices */
+#define PD_FLAG_WAIT_TIMEOUT 0x8      /* a copy pipeline wait passed its time limit; outputs invalid */
+
+/* Bytes at the start of every workspace that hold the status word. */
+#define PD_WORKSPACE_HEADER_BYTES 256
+
+/*
+ * Workspace bytes pd_paged_decode needs for this shape on the current device
+ * (the split-KV partial results and the status word). Depends on the
+ * device's SM count, so query it on the device that will run the call.
+ * Returns 0 on a bad shape or when no device is present (see
+ * pd_last_error_string()).
+ */
+size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                       pd_dtype dtype);
+
+/*
+ * Batched paged decode (batch_paged_decode.rs: BatchPagedDecodePlan::run and
+ * the per-dtype FFI launch it makes, whose argument order this follows).
+ *
+ * q, k_data, v_data, o: device, 16-byte aligned, layouts above.
+ * indices (may be NULL only if num_indices == 0), indptr, last_page_len: device int32.
+ * lse: device float32 [batch, num_qo_heads], natural log.
+ * head_dim: 64, 128 or 256. num_qo_heads % num_kv_heads == 0.
+ * num_total_pages: pages in k_data/v_data. num_indices: entries in indices
+ *   (the host-side length of the array; indptr[batch] must not exceed it).
+ * sm_scale: the score scale, used as given (typically 1/sqrt(head_dim)).
+ * workspace: device, 256-byte aligned, at least
+ *   pd_paged_decode_workspace_bytes(...) bytes, its header zeroed once by
+ *   pd_workspace_init() before first use. Calls that share a workspace must
+ *   be ordered on one stream.
+ *
+ * Long requests are split across warps in a load-balanced partition of all
+ * (kv head, page) work; partial (o, lse) pairs are combined by a merge
+ * kernel in a fixed order, so results do not depend on timing.
+ */
+pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data,
+                          const int32_t* indices, const int32_t* indptr,
+                          const int32_t* last_page_len, void* o, float* lse, int batch,
+                          int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                          int num_total_pages, int num_indices, float sm_scale, pd_dtype dtype,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Paged append (batch_paged_decode.rs, module doc "Companion plans":
+ * PagedKvAppendPlan writes the new K/V slices into the paged store at decode
+ * time; the caller owns the page table and its allocator).
+ *
+ * The caller first updates the page table for the new token: if request b's
+ * last page is full (or it has no page) it appends a free page to its list
+ * and sets last_page_len[b] = 1, otherwise it adds 1 to last_page_len[b].
+ * This call then copies, bit for bit, k_new[b, h, :] and v_new[b, h, :] into
+ * row last_page_len[b] - 1 of page indices[indptr[b+1] - 1], kv head h.
+ *
+ * k_new, v_new: device [batch, num_kv_heads, head_dim] T, 16-byte aligned.
+ * k_data, v_data: device, modified in place. indices/indptr/last_page_len:
+ *   device int32, the table after the caller's update.
+ * workspace: device, at least PD_WORKSPACE_HEADER_BYTES bytes (the status
+ *   word); a decode workspace may be shared.
+ * A request with no page, a page id out of range or a last_page_len outside
+ * [1, page_size] is skipped and flagged.
+ */
+pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, void* v_data,
+                          const int32_t* indices, const int32_t* indptr,
+                          const int32_t* last_page_len, int batch, int num_kv_heads, int head_dim,
+                          int page_size, int num_total_pages, int num_indices, pd_dtype dtype,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes pd_contiguous_decode needs (same rules as above). */
+size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads,
+                                            int head_dim, pd_dtype dtype);
+
+/*
+ * Decode over a contiguous cache (ferrum-kernels 0.7.7,
+ * src/backend/cuda/decode_attention.rs, decode_attention: q [num_q_heads,
+ * head_dim], k_cache/v_cache [num_kv_heads, max_kv_len, head_dim], rows
+ * [0, valid_kv_len) valid, scale), with a leading batch dimension:
+ *
+ * q, o: device [batch, num_qo_heads, head_dim] T, 16-byte aligned.
+ * k_cache, v_cache: device [batch, num_kv_heads, max_kv_len, head_dim] T.
+ * lse: device float32 [batch, num_qo_heads] or NULL to skip it.
+ * 0 <= valid_kv_len <= max_kv_len; valid_kv_len = 0 gives o = 0, lse = -inf.
+ * The same kernels as pd_paged_decode run with each request's rows taken as
+ * consecutive pages of one contiguous block.
+ */
+pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, int batch, int num_qo_heads, int num_kv_heads,
+                               int head_dim, int max_kv_len, int valid_kv_len, float sm_scale,
+                               pd_dtype dtype, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Merge attention states computed over disjoint key sets of the same query
+ * rows into the state over their union: lse = ln sum_c exp(lse_c),
+ * o = sum_c exp(lse_c - lse) * o_c, parts taken in index order. This is the
+ * combine step of the split-KV mode, exposed so that callers holding partial
+ * results from elsewhere (another device, another cache tier) can use it.
+ *
+ * o_parts: device float32 [num_parts, num_rows, head_dim] (each part already
+ *   normalised). lse_parts: device float32 [num_parts, num_rows], natural
+ *   log, -inf for an empty part. o: device [num_rows, head_dim] T, 16-byte
+ *   aligned. lse: device float32 [num_rows] or NULL. All parts empty gives
+ *   o = 0, lse = -inf.
+ */
+pd_status pd_merge_states(const float* o_parts, const float* lse_parts, int num_parts,
+                          int num_rows, int head_dim, void* o, float* lse, pd_dtype dtype,
+                          void* stream);
+
+/* Zero the status header of a workspace (enqueued on stream). */
+pd_status pd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read the sticky status word of a workspace into *flags (host). Synchronizes
+ * `stream`. The word is not cleared; pd_workspace_init() clears it.
+ */
+pd_status pd_read_device_flags(const void* workspace, int32_t* flags, void* stream);
+
+/*
+ * Plain device-to-device copy kernel (16-byte vector loads and stores, grid
+ * sized to the SM count), used to measure the achievable HBM bandwidth in
+ * the same process as the decode. dst and src: device, 16-byte aligned,
+ * not overlapping; bytes a multiple of 16.
+ */
+pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
+ * Kernel timing for measurement. While enabled, every decode call records
+ * CUDA events on its stream around its decode kernel and its merge kernel.
+ * pd_profile_read() synchronizes on those events, returns the summed
+ * milliseconds and launch counts since the last read, and starts a new
+ * count. Enabling costs two event records per kernel; it is off by default.
+ */
+pd_status pd_profile_enable(int enable);
+pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms,
+                          int* merge_launches);
+
+/* Message for the last error status returned on this host thread ("" if none). */
+const char* pd_last_error_string(void);
+
+/* PD_VERSION of the built library. */
+int pd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDECODE_H */

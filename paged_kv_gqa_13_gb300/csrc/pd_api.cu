@@ -1,0 +1,544 @@
+// The C ABI of pagedecode: argument checks, planning of the work partition,
+// kernel launches, the paged append and copy kernels, profiling hooks.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/pagedecode.h"
+#include "pd_decode.cuh"
+
+namespace pd {
+bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks);
+bool lookup_kernels_f16(int head_dim, int heads, KernelSet* ks);
+bool lookup_kernels_bf16(int head_dim, int heads, KernelSet* ks);
+}  // namespace pd
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+pd_status fail(pd_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pd_status fail(pd_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pd_status ok() {
+    g_err[0] = '\0';
+    return PD_OK;
+}
+
+pd_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_size(pd_dtype dt) { return dt == PD_F32 ? 4 : 2; }
+
+bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
+    switch (dt) {
+        case PD_F32: return pd::lookup_kernels_f32(D, G, ks);
+        case PD_F16: return pd::lookup_kernels_f16(D, G, ks);
+        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks);
+    }
+    return false;
+}
+
+// Per-device facts, read once.
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem = 0;
+};
+
+std::mutex g_mu;
+
+pd_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    static std::vector<DeviceInfo> cache;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int(cache.size()) <= dev) cache.resize(dev + 1);
+    if (cache[dev].sms == 0) {
+        int sms = 0, smem = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        cache[dev].sms = sms;
+        cache[dev].max_smem = smem;
+    }
+    *out = cache[dev];
+    return PD_OK;
+}
+
+// Raise a kernel's dynamic shared memory limit once per (device, kernel, size).
+pd_status allow_smem(const void* fn, int bytes) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    struct Entry {
+        int dev;
+        const void* fn;
+        int bytes;
+    };
+    static std::vector<Entry> done;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (const Entry& x : done)
+            if (x.dev == dev && x.fn == fn && x.bytes >= bytes) return PD_OK;
+    }
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    std::lock_guard<std::mutex> lk(g_mu);
+    done.push_back({dev, fn, bytes});
+    return PD_OK;
+}
+
+// How a decode call is laid out on the device.
+struct Plan {
+    int group = 0, head_tiles = 0, heads_per_tile = 0, G = 0;
+    pd::KernelSet ks{};
+    int table_bytes = 0, nwarps = 0, ctas = 0;
+    long long total_warps = 0, segments = 0, slots = 0;
+    size_t smem = 0, lse_off = 0, o_off = 0, ws_bytes = 0;
+};
+
+// Smallest number of head tiles that splits the group into tiles of <= 8 heads.
+void split_group(int g, int* tiles, int* per) {
+    int t = 1;
+    while (g / t > 8 || g % t != 0) ++t;
+    *tiles = t;
+    *per = g / t;
+}
+
+pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p) {
+    if (dt != PD_F32 && dt != PD_F16 && dt != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (batch <= 0 || Hq <= 0 || Hk <= 0) return fail(PD_ERR_INVALID, "batch, num_qo_heads and num_kv_heads must be positive");
+    if (Hq % Hk != 0) return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", Hq, Hk);
+    if (D != 64 && D != 128 && D != 256) return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", D);
+    p->group = Hq / Hk;
+    split_group(p->group, &p->head_tiles, &p->heads_per_tile);
+    p->G = 1;
+    while (p->G < p->heads_per_tile) p->G *= 2;
+    if (!lookup(dt, D, p->G, &p->ks)) return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
+    DeviceInfo di;
+    pd_status st = device_info(&di);
+    if (st != PD_OK) return st;
+    p->table_bytes = pd::table_bytes_for(!contiguous && batch <= pd::kTableMax);
+    p->nwarps = (di.max_smem - p->table_bytes) / p->ks.warp_bytes;
+    if (p->nwarps > 8) p->nwarps = 8;
+    if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
+    p->smem = size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
+    if ((st = allow_smem(p->ks.decode, int(p->smem))) != PD_OK) return st;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->ks.decode, p->nwarps * 32, p->smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (per_sm < 1) per_sm = 1;
+    p->ctas = di.sms * per_sm;
+    p->total_warps = (long long)p->ctas * p->nwarps;
+    p->segments = (long long)p->head_tiles * Hk * batch;
+    p->slots = p->total_warps + p->segments;
+    p->lse_off = PD_WORKSPACE_HEADER_BYTES;
+    p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
+    p->ws_bytes = p->o_off + size_t(p->slots) * p->G * D * 4;
+    return PD_OK;
+}
+
+// ---------------------------------------------------------------- profiling
+
+struct Profile {
+    bool on = false;
+    std::vector<cudaEvent_t> free_events;
+    std::vector<cudaEvent_t> decode_marks;  // pairs: start, end
+    std::vector<cudaEvent_t> merge_marks;
+};
+Profile g_prof;
+std::mutex g_prof_mu;
+
+cudaEvent_t take_event() {
+    if (g_prof.free_events.empty()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        return e;
+    }
+    cudaEvent_t e = g_prof.free_events.back();
+    g_prof.free_events.pop_back();
+    return e;
+}
+
+void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
+    cudaEvent_t e = take_event();
+    if (e != nullptr) {
+        cudaEventRecord(e, s);
+        v->push_back(e);
+    }
+}
+
+// ---------------------------------------------------------------- decode launch
+
+pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, cudaStream_t stream) {
+    std::unique_lock<std::mutex> plk(g_prof_mu);
+    const bool prof = g_prof.on;
+    if (!prof) plk.unlock();
+    cudaError_t e;
+    if (a.total_pos > 0) {
+        a.pos_per_warp = (a.total_pos + pl.total_warps - 1) / pl.total_warps;
+        const long long warps_used = (a.total_pos + a.pos_per_warp - 1) / a.pos_per_warp;
+        const int grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(pl.nwarps * 32);
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = stream;
+        void* args[] = {&a};
+        if (prof) mark(&g_prof.decode_marks, stream);
+        e = cudaLaunchKernelExC(&cfg, pl.ks.decode, args);
+        if (prof) mark(&g_prof.decode_marks, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    } else {
+        a.pos_per_warp = 1;
+    }
+    pd::MergeArgs m{};
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.indptr = a.indptr;
+    m.o = a.o;
+    m.lse = a.lse;
+    m.flags = a.flags;
+    m.batch = a.batch;
+    m.num_qo_heads = a.num_qo_heads;
+    m.num_kv_heads = a.num_kv_heads;
+    m.group = a.group;
+    m.head_tiles = a.head_tiles;
+    m.heads_per_tile = a.heads_per_tile;
+    m.G = pl.G;
+    m.n_pos = a.n_pos;
+    m.pos_per_warp = a.pos_per_warp;
+    m.contiguous = a.contiguous;
+    m.npv = a.npv;
+    const long long pairs = pl.segments * pl.heads_per_tile;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned((pairs + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* margs[] = {&m};
+    if (prof) mark(&g_prof.merge_marks, stream);
+    e = cudaLaunchKernelExC(&cfg, pl.ks.merge, margs);
+    if (prof) mark(&g_prof.merge_marks, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    (void)D;
+    return ok();
+}
+
+// ---------------------------------------------------------------- append / copy kernels
+
+// One warp per (request, kv head): copy the new K and V rows into their slot.
+__global__ void __launch_bounds__(128) append_kernel(const uint8_t* k_new, const uint8_t* v_new, uint8_t* k_data,
+                                                     uint8_t* v_data, const int32_t* indices, const int32_t* indptr,
+                                                     const int32_t* last_page_len, int batch, int Hk, int row_bytes,
+                                                     int page_size, int num_total_pages, int num_indices, int* flags) {
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (w >= (long long)batch * Hk) return;
+    const int b = int(w / Hk), kh = int(w % Hk);
+    const int lo = __ldg(indptr + b), hi = __ldg(indptr + b + 1);
+    if (hi <= lo || lo < 0 || hi > num_indices) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadIndptr);
+        return;
+    }
+    const int page = __ldg(indices + hi - 1);
+    const int slot = __ldg(last_page_len + b) - 1;
+    if (page < 0 || page >= num_total_pages) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadPage);
+        return;
+    }
+    if (slot < 0 || slot >= page_size) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadLastPageLen);
+        return;
+    }
+    const size_t dst = ((size_t(page) * Hk + kh) * page_size + slot) * size_t(row_bytes);
+    const size_t src = (size_t(b) * Hk + kh) * size_t(row_bytes);
+    for (int off = lane * 16; off < row_bytes; off += 32 * 16) {
+        *reinterpret_cast<uint4*>(k_data + dst + off) = __ldg(reinterpret_cast<const uint4*>(k_new + src + off));
+        *reinterpret_cast<uint4*>(v_data + dst + off) = __ldg(reinterpret_cast<const uint4*>(v_new + src + off));
+    }
+}
+
+// Plain streaming copy: four independent 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(512) copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n) {
+    const size_t stride = size_t(gridDim.x) * blockDim.x;
+    size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride), c = __ldcs(src + i + 2 * stride),
+                    d = __ldcs(src + i + 3 * stride);
+        __stcs(dst + i, a);
+        __stcs(dst + i + stride, b);
+        __stcs(dst + i + 2 * stride, c);
+        __stcs(dst + i + 3 * stride, d);
+    }
+    for (; i < n; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+pd_status check_workspace(void* ws, size_t have, size_t need) {
+    if (ws == nullptr) return fail(PD_ERR_WORKSPACE, "workspace is null (needed %zu bytes)", need);
+    if (!aligned(ws, 256)) return fail(PD_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+    if (have < need) return fail(PD_ERR_WORKSPACE, "workspace too small: needed %zu bytes, got %zu", need, have);
+    return PD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pd_version(void) { return PD_VERSION; }
+
+const char* pd_last_error_string(void) { return g_err; }
+
+size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim, pd_dtype dtype) {
+    Plan p;
+    if (make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &p) != PD_OK) return 0;
+    ok();
+    return p.ws_bytes;
+}
+
+size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                            pd_dtype dtype) {
+    Plan p;
+    if (make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, &p) != PD_OK) return 0;
+    ok();
+    return p.ws_bytes;
+}
+
+pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data, const int32_t* indices,
+                          const int32_t* indptr, const int32_t* last_page_len, void* o, float* lse, int batch,
+                          int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_total_pages,
+                          int num_indices, float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0)
+        return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads, page_size and num_total_pages must be positive");
+    if (num_indices < 0) return fail(PD_ERR_INVALID, "num_indices must not be negative");
+    if (num_qo_heads % num_kv_heads != 0)
+        return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", num_qo_heads, num_kv_heads);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!std::isfinite(sm_scale)) return fail(PD_ERR_INVALID, "sm_scale must be finite");
+    if (!q || !k_data || !v_data || !indptr || !last_page_len || !o || !lse || (num_indices > 0 && !indices))
+        return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(q, 16) || !aligned(k_data, 16) || !aligned(v_data, 16) || !aligned(o, 16))
+        return fail(PD_ERR_UNSUPPORTED, "q, k_data, v_data and o must be 16-byte aligned");
+    if (!aligned(lse, 4) || !aligned(indptr, 4) || !aligned(last_page_len, 4) || (indices && !aligned(indices, 4)))
+        return fail(PD_ERR_UNSUPPORTED, "lse, indices, indptr and last_page_len must be 4-byte aligned");
+    Plan pl;
+    pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl);
+    if (st != PD_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, pl.ws_bytes)) != PD_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    pd::DecodeArgs a{};
+    a.q = q;
+    a.k = k_data;
+    a.v = v_data;
+    a.indices = indices;
+    a.indptr = indptr;
+    a.last_page_len = last_page_len;
+    a.o = o;
+    a.lse = lse;
+    a.part_lse = reinterpret_cast<float*>(ws + pl.lse_off);
+    a.part_o = reinterpret_cast<float*>(ws + pl.o_off);
+    a.flags = reinterpret_cast<int*>(ws);
+    a.batch = batch;
+    a.num_qo_heads = num_qo_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.page_size = page_size;
+    a.num_total_pages = num_total_pages;
+    a.group = pl.group;
+    a.head_tiles = pl.head_tiles;
+    a.heads_per_tile = pl.heads_per_tile;
+    a.n_pos = num_indices;
+    a.table_bytes = pl.table_bytes;
+    a.total_pos = (long long)pl.head_tiles * num_kv_heads * num_indices;
+    a.q_scale = sm_scale * pd::kLog2e;
+    a.contiguous = 0;
+    return launch_decode(pl, a, head_dim, static_cast<cudaStream_t>(stream));
+}
+
+pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int batch,
+                               int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
+                               float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || max_kv_len <= 0)
+        return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads and max_kv_len must be positive");
+    if (valid_kv_len < 0 || valid_kv_len > max_kv_len)
+        return fail(PD_ERR_INVALID, "valid_kv_len (%d) must be in [0, max_kv_len=%d]", valid_kv_len, max_kv_len);
+    if (num_qo_heads % num_kv_heads != 0)
+        return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", num_qo_heads, num_kv_heads);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!std::isfinite(sm_scale)) return fail(PD_ERR_INVALID, "sm_scale must be finite");
+    if (!q || !k_cache || !v_cache || !o) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16))
+        return fail(PD_ERR_UNSUPPORTED, "q, k_cache, v_cache and o must be 16-byte aligned");
+    if (lse && !aligned(lse, 4)) return fail(PD_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+    Plan pl;
+    pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, &pl);
+    if (st != PD_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, pl.ws_bytes)) != PD_OK) return st;
+    const int vpage = 4 * pl.ks.rows_per_stage;  // rows per work position
+    const int npv = (valid_kv_len + vpage - 1) / vpage;
+    const long long n_pos = (long long)batch * npv;
+    if (n_pos > 0x7fffffffLL) return fail(PD_ERR_UNSUPPORTED, "batch * max_kv_len too large");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    pd::DecodeArgs a{};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.o = o;
+    a.lse = lse;
+    a.part_lse = reinterpret_cast<float*>(ws + pl.lse_off);
+    a.part_o = reinterpret_cast<float*>(ws + pl.o_off);
+    a.flags = reinterpret_cast<int*>(ws);
+    a.batch = batch;
+    a.num_qo_heads = num_qo_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.page_size = vpage;
+    a.num_total_pages = 1;
+    a.group = pl.group;
+    a.head_tiles = pl.head_tiles;
+    a.heads_per_tile = pl.heads_per_tile;
+    a.n_pos = int(n_pos);
+    a.table_bytes = 0;
+    a.total_pos = (long long)pl.head_tiles * num_kv_heads * n_pos;
+    a.q_scale = sm_scale * pd::kLog2e;
+    a.contiguous = 1;
+    a.max_kv_len = max_kv_len;
+    a.valid_kv_len = valid_kv_len;
+    a.vpage = vpage;
+    a.npv = npv;
+    return launch_decode(pl, a, head_dim, static_cast<cudaStream_t>(stream));
+}
+
+pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, void* v_data, const int32_t* indices,
+                          const int32_t* indptr, const int32_t* last_page_len, int batch, int num_kv_heads,
+                          int head_dim, int page_size, int num_total_pages, int num_indices, pd_dtype dtype,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (batch <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0 || num_indices < 0)
+        return fail(PD_ERR_INVALID, "batch, num_kv_heads, page_size and num_total_pages must be positive");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!k_new || !v_new || !k_data || !v_data || !indptr || !last_page_len || (num_indices > 0 && !indices))
+        return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_data, 16) || !aligned(v_data, 16))
+        return fail(PD_ERR_UNSUPPORTED, "k_new, v_new, k_data and v_data must be 16-byte aligned");
+    pd_status st = check_workspace(workspace, workspace_bytes, PD_WORKSPACE_HEADER_BYTES);
+    if (st != PD_OK) return st;
+    const long long warps = (long long)batch * num_kv_heads;
+    append_kernel<<<unsigned((warps + 3) / 4), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), static_cast<uint8_t*>(k_data),
+        static_cast<uint8_t*>(v_data), indices, indptr, last_page_len, batch, num_kv_heads,
+        int(head_dim * elem_size(dtype)), page_size, num_total_pages, num_indices, static_cast<int*>(workspace));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return ok();
+}
+
+pd_status pd_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int num_rows, int head_dim,
+                          void* o, float* lse, pd_dtype dtype, void* stream) {
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (num_parts <= 0 || num_rows < 0) return fail(PD_ERR_INVALID, "num_parts must be positive and num_rows not negative");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!o_parts || !lse_parts || !o) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(o_parts, 16) || !aligned(o, 16)) return fail(PD_ERR_UNSUPPORTED, "o_parts and o must be 16-byte aligned");
+    if (num_rows == 0) return ok();
+    pd::KernelSet ks{};
+    if (!lookup(dtype, head_dim, 1, &ks)) return fail(PD_ERR_UNSUPPORTED, "no merge kernel for this head_dim");
+    const void* fn = ks.merge_states;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned((num_rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    void* args[] = {&o_parts, &lse_parts, &num_parts, &num_rows, &o, &lse};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return cuda_fail(e, "merge_states launch");
+    return ok();
+}
+
+pd_status pd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    pd_status st = check_workspace(workspace, workspace_bytes, PD_WORKSPACE_HEADER_BYTES);
+    if (st != PD_OK) return st;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, PD_WORKSPACE_HEADER_BYTES, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
+}
+
+pd_status pd_read_device_flags(const void* workspace, int32_t* flags, void* stream) {
+    if (!workspace || !flags) return fail(PD_ERR_INVALID, "null pointer argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    return ok();
+}
+
+pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream) {
+    if (!dst || !src) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(dst, 16) || !aligned(src, 16) || bytes % 16 != 0)
+        return fail(PD_ERR_UNSUPPORTED, "dst, src and bytes must be multiples of 16");
+    if (bytes == 0) return ok();
+    DeviceInfo di;
+    pd_status st = device_info(&di);
+    if (st != PD_OK) return st;
+    copy_kernel<<<di.sms * 4, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+    return ok();
+}
+
+pd_status pd_profile_enable(int enable) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.on = enable != 0;
+    return ok();
+}
+
+pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms, int* merge_launches) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    auto sum = [](std::vector<cudaEvent_t>& v, double* ms, int* n) -> cudaError_t {
+        double t = 0;
+        int cnt = 0;
+        cudaError_t err = cudaSuccess;
+        for (size_t i = 0; i + 1 < v.size(); i += 2) {
+            float x = 0;
+            err = cudaEventSynchronize(v[i + 1]);
+            if (err == cudaSuccess) err = cudaEventElapsedTime(&x, v[i], v[i + 1]);
+            if (err != cudaSuccess) break;
+            t += x;
+            ++cnt;
+        }
+        for (cudaEvent_t e : v) g_prof.free_events.push_back(e);
+        v.clear();
+        if (ms) *ms = t;
+        if (n) *n = cnt;
+        return err;
+    };
+    cudaError_t e1 = sum(g_prof.decode_marks, decode_ms, decode_launches);
+    cudaError_t e2 = sum(g_prof.merge_marks, merge_ms, merge_launches);
+    if (e1 != cudaSuccess) return cuda_fail(e1, "reading decode events");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "reading merge events");
+    return ok();
+}
+
+}  // extern "C"

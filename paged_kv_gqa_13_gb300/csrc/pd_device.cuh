@@ -1,0 +1,286 @@
+// Device-side building blocks shared by the pagedecode kernels: PTX wrappers
+// for mbarriers, bulk async copies and programmatic dependent launch, element
+// conversions, warp reductions and the kernel argument blocks.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pd {
+
+// Status word bits (the same values as PD_FLAG_* in pagedecode.h).
+constexpr int kFlagBadPage = 0x1;
+constexpr int kFlagBadLastPageLen = 0x2;
+constexpr int kFlagBadIndptr = 0x4;
+constexpr int kFlagTimeout = 0x8;
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// Upper bound on one pipeline wait. Copies of a few KB finish in
+// microseconds; this only ends a wait that can never finish.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of a barrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk async copy global -> shared, completion counted on `bar` in bytes.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// 2^x on the special-function unit; inputs far below 0 give +0, -inf gives +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- elements
+
+template <typename T>
+struct Elt;
+
+template <>
+struct Elt<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static __forceinline__ void to_f32(const uint4& r, float* f) {
+        f[0] = __uint_as_float(r.x);
+        f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z);
+        f[3] = __uint_as_float(r.w);
+    }
+    __device__ static __forceinline__ uint4 from_f32(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+template <>
+struct Elt<__half> {
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ float2 pair(uint32_t w) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+    __device__ static __forceinline__ void to_f32(const uint4& r, float* f) {
+        float2 a = pair(r.x), b = pair(r.y), c = pair(r.z), d = pair(r.w);
+        f[0] = a.x, f[1] = a.y, f[2] = b.x, f[3] = b.y, f[4] = c.x, f[5] = c.y, f[6] = d.x, f[7] = d.y;
+    }
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ static __forceinline__ uint4 from_f32(const float* f) {
+        return make_uint4(pack(f[0], f[1]), pack(f[2], f[3]), pack(f[4], f[5]), pack(f[6], f[7]));
+    }
+};
+
+template <>
+struct Elt<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    // A bfloat16 is the upper half of a float: widening is a shift or a mask.
+    __device__ static __forceinline__ void to_f32(const uint4& r, float* f) {
+        f[0] = __uint_as_float(r.x << 16), f[1] = __uint_as_float(r.x & 0xffff0000u);
+        f[2] = __uint_as_float(r.y << 16), f[3] = __uint_as_float(r.y & 0xffff0000u);
+        f[4] = __uint_as_float(r.z << 16), f[5] = __uint_as_float(r.z & 0xffff0000u);
+        f[6] = __uint_as_float(r.w << 16), f[7] = __uint_as_float(r.w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ static __forceinline__ uint4 from_f32(const float* f) {
+        return make_uint4(pack(f[0], f[1]), pack(f[2], f[3]), pack(f[4], f[5]), pack(f[6], f[7]));
+    }
+};
+
+// ---------------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+    return x;
+}
+
+// Reduce-scatter of N partial sums across the lanes that differ in the bits
+// below 2*OFF (a "row group"). At each level the lane keeps half of its
+// values and adds the partner's copy of that half; once one value is left the
+// remaining levels are plain butterflies. Total shuffles: N/2 + N/4 + ... per
+// lane instead of N * log2(lanes) for N separate all-reduces.
+template <int N, int OFF>
+struct ReduceScatter {
+    __device__ static __forceinline__ void run(float* v, int lane) {
+        if constexpr (OFF == 0) {
+            return;
+        } else if constexpr (N >= 2) {
+            constexpr int H = N / 2;
+            const bool up = (lane & OFF) != 0;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const float send = up ? v[j] : v[j + H];
+                const float keep = up ? v[j + H] : v[j];
+                v[j] = keep + __shfl_xor_sync(kFull, send, OFF);
+            }
+            ReduceScatter<H, OFF / 2>::run(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(kFull, v[0], OFF);
+            ReduceScatter<1, OFF / 2>::run(v, lane);
+        }
+    }
+    // Which of the original N values v[j] holds after run().
+    __device__ static __forceinline__ int index(int j, int lane) {
+        if constexpr (OFF == 0 || N < 2) {
+            return j;
+        } else {
+            return ReduceScatter<N / 2, OFF / 2>::index(j, lane) + (((lane & OFF) != 0) ? N / 2 : 0);
+        }
+    }
+};
+
+// ---------------------------------------------------------------- arguments
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* indices;
+    const int32_t* indptr;
+    const int32_t* last_page_len;
+    void* o;
+    float* lse;       // may be null (contiguous entry)
+    float* part_o;    // [slots][G][D] f32, normalised partial outputs
+    float* part_lse;  // [slots][G] f32, partial lse in log2 units
+    int* flags;       // sticky status word
+    int batch, num_qo_heads, num_kv_heads, page_size, num_total_pages;
+    int group, head_tiles, heads_per_tile;
+    int n_pos;                 // positions per (kv head, head tile) pass
+    int table_bytes;           // dynamic smem bytes holding the staged indptr/last_page_len
+    long long total_pos;       // head_tiles * num_kv_heads * n_pos
+    long long pos_per_warp;
+    float q_scale;             // sm_scale * log2(e)
+    int contiguous;            // 0: paged store, 1: contiguous cache
+    long long max_kv_len;      // contiguous: rows per (request, kv head) block
+    int valid_kv_len, vpage, npv;  // contiguous: valid rows, rows per virtual page, pages per request
+};
+
+struct MergeArgs {
+    const float* part_o;
+    const float* part_lse;
+    const int32_t* indptr;
+    void* o;
+    float* lse;
+    int* flags;
+    int batch, num_qo_heads, num_kv_heads, group, head_tiles, heads_per_tile, G;
+    int n_pos;
+    long long pos_per_warp;
+    int contiguous, npv;
+};
+
+// Position range [lo, hi) of request b within one pass over the positions.
+// Shared by the decode walk and the merge so that both cut identically.
+__device__ __forceinline__ void request_range(int b, int n_pos, bool contiguous, int npv, int raw_lo,
+                                              int raw_hi, int* lo, int* hi) {
+    if (contiguous) {
+        *lo = b * npv;
+        *hi = (b + 1) * npv;
+        return;
+    }
+    int l = raw_lo < 0 ? 0 : (raw_lo > n_pos ? n_pos : raw_lo);
+    int h = raw_hi > n_pos ? n_pos : raw_hi;
+    *lo = l;
+    *hi = h < l ? l : h;
+}
+
+}  // namespace pd

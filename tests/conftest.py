@@ -31,8 +31,6 @@ def pytest_collection_modifyitems(config, items):
 
 @pytest.fixture(scope="session", autouse=True)
 def _built():
-    import oracle
-    import workloads
+    import __graft_entry__
 
-    workloads.build()
-    oracle.build()
+    __graft_entry__.build()

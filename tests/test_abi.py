@@ -1,0 +1,89 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects malformed arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedecode.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared()
+    for n in ("pd_paged_decode", "pd_paged_append", "pd_contiguous_decode", "pd_merge_states",
+              "pd_paged_decode_workspace_bytes", "pd_last_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    import paged_kv_gqa_13_gb300 as pd
+
+    lib = ctypes.CDLL(pd.LIBRARY_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert set(_declared()) == set(pd.EXPORTED)
+    assert pd.pd_version() == 1
+
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced: every call below fails its checks first
+
+
+def _decode(**kw):
+    import paged_kv_gqa_13_gb300 as pd
+
+    args = dict(q=FAKE, k=FAKE, v=FAKE, indices=FAKE, indptr=FAKE, lpl=FAKE, o=FAKE, lse=FAKE, batch=2,
+                hq=8, hk=2, d=128, p=16, pages=10, nidx=4, scale=0.1, dtype=pd.PD_BF16, ws=FAKE,
+                wsb=1 << 20, stream=None)
+    args.update(kw)
+    return pd._lib.pd_paged_decode(*args.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=0), 1), (dict(hq=0), 1), (dict(hk=-1), 1), (dict(p=0), 1), (dict(pages=0), 1),
+    (dict(nidx=-1), 1), (dict(hq=9), 1), (dict(d=96), 2), (dict(d=512), 2), (dict(dtype=7), 2),
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(indices=None), 1), (dict(o=FAKE + 8), 2),
+    (dict(k=FAKE + 4), 2), (dict(indptr=FAKE + 2), 2), (dict(scale=float("nan")), 1),
+])
+def test_paged_decode_rejects_bad_arguments(kw, status):
+    import paged_kv_gqa_13_gb300 as pd
+
+    assert _decode(**kw) == status
+    assert pd.pd_last_error_string() != ""
+
+
+def test_indices_may_be_null_when_empty():
+    import paged_kv_gqa_13_gb300 as pd
+
+    # Passes the argument checks; then stops at the device query (no GPU) or at the
+    # too-small fake workspace (GPU present). Nothing is launched either way.
+    st = _decode(indices=None, nidx=0, wsb=4096)
+    assert st in (pd.PD_ERR_CUDA, pd.PD_ERR_WORKSPACE)
+
+
+def test_contiguous_and_append_and_merge_reject_bad_arguments():
+    import paged_kv_gqa_13_gb300 as pd
+
+    L = pd._lib
+    # valid_kv_len > max_kv_len
+    assert L.pd_contiguous_decode(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 128, 10, 11, 0.1, pd.PD_F16, FAKE,
+                                  1 << 20, None) == pd.PD_ERR_INVALID
+    assert L.pd_contiguous_decode(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 80, 10, 5, 0.1, pd.PD_F16, FAKE,
+                                  1 << 20, None) == pd.PD_ERR_UNSUPPORTED
+    assert L.pd_paged_append(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 10, 4, pd.PD_F16, FAKE,
+                             256, None) == pd.PD_ERR_INVALID
+    assert L.pd_paged_append(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 16, 10, 4, pd.PD_F16, None,
+                             0, None) == pd.PD_ERR_WORKSPACE
+    assert L.pd_paged_append(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 16, 10, 4, pd.PD_F16, FAKE,
+                             16, None) == pd.PD_ERR_WORKSPACE
+    assert L.pd_merge_states(FAKE, FAKE, 0, 4, 128, FAKE, None, pd.PD_F32, None) == pd.PD_ERR_INVALID
+    assert L.pd_merge_states(FAKE, FAKE, 2, 4, 100, FAKE, None, pd.PD_F32, None) == pd.PD_ERR_UNSUPPORTED
+    assert L.pd_copy_bytes(FAKE, FAKE, 10, None) == pd.PD_ERR_UNSUPPORTED
+    assert L.pd_workspace_init(FAKE, 8, None) == pd.PD_ERR_WORKSPACE

@@ -1,0 +1,75 @@
+"""GPU parity for pd_paged_append: bit-exact against the oracle's host mirror,
+then append-then-decode steps against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_helpers import DeviceWorkload, compare, table_dev, to_dev, to_host_raw
+
+pytestmark = pytest.mark.gpu
+
+
+def _append_steps(w, steps, check_pool_every=1):
+    import paged_kv_gqa_13_gb300 as pd
+
+    dw = DeviceWorkload(w)
+    k_host, v_host = w.k_data.copy(), w.v_data.copy()
+    t = w.table
+    for step in range(steps):
+        t = wl.table_after_append(t)
+        kn, vn = w.new_rows(step)
+        dw.set_table(t)
+        pd.pd_paged_append(to_dev(kn, w.dtype), to_dev(vn, w.dtype), dw.k, dw.v, dw.indices, dw.indptr,
+                           dw.lpl, dw.ws)
+        oracle.paged_append(kn, vn, k_host, v_host, t.indices, t.indptr, t.last_page_len, w.dtype)
+        if step % check_pool_every == 0 or step == steps - 1:
+            assert np.array_equal(to_host_raw(dw.k, w.dtype), k_host), f"K pool differs after step {step}"
+            assert np.array_equal(to_host_raw(dw.v, w.dtype), v_host), f"V pool differs after step {step}"
+        o, lse = dw.decode()
+        o_ref, lse_ref = oracle.paged_decode(w.q, k_host, v_host, t.indices, t.indptr, t.last_page_len,
+                                             w.num_qo_heads, w.num_kv_heads, w.head_dim, t.page_size,
+                                             w.sm_scale, w.dtype)
+        compare(o, lse, o_ref, lse_ref, w.dtype, f"step {step}")
+    assert dw.flags() == 0
+    return dw
+
+
+def test_append_then_decode_mha_d256():
+    # Lengths near page boundaries so appends open fresh pages in several steps.
+    w = wl.make_paged("append_small", "f16", [15, 16, 1, 31, 47, 200, 3, 64], 16, 16, 256, 16, seed=80,
+                      extra_rows=8, append_steps=8)
+    _append_steps(w, 8)
+
+
+@pytest.mark.parametrize("dtype,head_dim", [("bf16", 128), ("f32", 64), ("f16", 64)])
+def test_append_gqa_shapes(dtype, head_dim):
+    w = wl.make_paged(f"append_{dtype}", dtype, [0, 5, 16, 33], 8, 2, head_dim, 16, seed=81, extra_rows=3,
+                      append_steps=3)
+    _append_steps(w, 3)
+
+
+def test_append_flags_bad_tables():
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("append_bad", "bf16", [5, 5], 8, 2, 128, 16, seed=82, extra_rows=1)
+    dw = DeviceWorkload(w)
+    kn, vn = w.new_rows(0)
+    kd, vd = to_dev(kn, "bf16"), to_dev(vn, "bf16")
+    before = dw.k.clone()
+    t = wl.table_after_append(w.table)
+    t.indices[t.indptr[1] - 1] = -3  # bad page id for request 0
+    ind, ptr, lpl = table_dev(t)
+    pd.pd_paged_append(kd, vd, dw.k, dw.v, ind, ptr, lpl, dw.ws)
+    assert dw.flags() & pd.PD_FLAG_BAD_PAGE_ID
+    pd.pd_workspace_init(dw.ws)
+    t = wl.table_after_append(w.table)
+    t.last_page_len[1] = 0  # slot -1
+    ind, ptr, lpl = table_dev(t)
+    pd.pd_paged_append(kd, vd, dw.k, dw.v, ind, ptr, lpl, dw.ws)
+    assert dw.flags() & pd.PD_FLAG_BAD_LAST_PAGE_LEN
+    # request 0 (good) was written in the second call, request 1 was not
+    changed = (dw.k.view(torch.int16) != before.view(torch.int16)).any(dim=-1).nonzero()
+    assert len(changed) == w.num_kv_heads
