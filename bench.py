@@ -219,18 +219,20 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     # in-process copy-kernel bandwidth (reported beside the driver's measured peak)
-    src = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
-    dst = torch.empty_like(src)
-    for _ in range(3):
-        pd.pd_copy_bytes(dst, src)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(10):
-        pd.pd_copy_bytes(dst, src)
-    e1.record()
-    torch.cuda.synchronize()
-    copy_gbs = 2 * src.numel() * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
-    del src, dst
+    copy_gbs = None
+    if not args.quick:
+        src = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            pd.pd_copy_bytes(dst, src)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            pd.pd_copy_bytes(dst, src)
+        e1.record()
+        torch.cuda.synchronize()
+        copy_gbs = 2 * src.numel() * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del src, dst
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     entries = [x.strip() for x in visible.split(",") if x.strip()]
@@ -267,7 +269,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     # end to end through the C ABI with host buffers: per step, copy q and the
     # page table in from pinned host memory, decode, copy o and lse out.
     e2e = None
-    if mode == "paged" and not w.append_steps:
+    if mode == "paged" and not w.append_steps and not args.quick:
         t = tables[0]
         hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16 if w.dtype != "f32" else np.float32)).pin_memory()
         h_ind = torch.from_numpy(t.indices.astype(np.int32)).pin_memory()
@@ -339,6 +341,8 @@ def main():
                              "mha_append"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="decode steps only: no copy-peak, end-to-end or CPU-baseline legs (for profiler runs)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -392,7 +396,7 @@ def main():
                 "peak_source": peaks["source"], "kernel": "decode_kernel",
                 "kernel_us": dec_ms * 1e3, "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
                 "copy_kernel_gbs": r["copy_gbs"]}
-    cb = None if args.no_cpu_baseline else cpu_baseline(w, r["mode"])
+    cb = None if (args.no_cpu_baseline or args.quick) else cpu_baseline(w, r["mode"])
     launches = prof["decode_launches"] + prof["merge_launches"] + (args.steps if w.append_steps else 0)
     ms = r["ms_all"]
     line = {
