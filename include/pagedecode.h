@@ -207,6 +207,37 @@ pd_status pd_profile_enable(int enable);
 pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms,
                           int* merge_launches);
 
+/*
+ * pd_paged_decode for callers that cannot allocate device memory at call
+ * time (no counterpart on the pages: it is a deployment variant of the call
+ * above). Typical callers: a plugin inside a host engine that owns all
+ * device memory and passes its ops no scratch, or a serving loop that may
+ * not call cudaMalloc on its hot path. Arguments are those of
+ * pd_paged_decode without the workspace.
+ *
+ * The split-KV scratch lives in a 16 MiB static device array inside this
+ * library, which every device that loads the library holds until the
+ * process exits. A shape whose scratch (pd_paged_decode_workspace_bytes)
+ * exceeds 16 MiB is rejected with PD_ERR_WORKSPACE before anything is
+ * enqueued; the bundled workload shapes need at most ~13 MiB on a 148-SM
+ * GB300. This call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Each call clears the status word, then runs
+ * the decode; the kernels' device-side table checks still run, but this
+ * variant gives no way to read their flags. All calls share one array, so
+ * calls whose kernels overlap on the GPU (different streams, or different
+ * host threads) race on it: order them on one stream.
+ */
+pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, const void* v_data,
+                                  const int32_t* indices, const int32_t* indptr,
+                                  const int32_t* last_page_len, void* o, float* lse, int batch,
+                                  int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                                  int num_total_pages, int num_indices, float sm_scale,
+                                  pd_dtype dtype, void* stream);
+
 /* Message for the last error status returned on this host thread ("" if none). */
 const char* pd_last_error_string(void);
 

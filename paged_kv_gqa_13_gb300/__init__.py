@@ -49,6 +49,7 @@ _SIGS = {
     "pd_profile_enable": (_I, [_I]),
     "pd_profile_read": (_I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+    "pd_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pd_last_error_string": (ctypes.c_char_p, []),
     "pd_version": (_I, []),
 }
@@ -149,6 +150,21 @@ def pd_paged_decode(q, k_data, v_data, indices, indptr, last_page_len, o, lse, s
         _ptr(last_page_len), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
         num_total_pages, indices.numel(), float(sm_scale), _dtype_code(q), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+
+
+def pd_paged_decode_noalloc(q, k_data, v_data, indices, indptr, last_page_len, o, lse, sm_scale: float,
+                            stream=None) -> None:
+    """pd_paged_decode with the library's built-in 16 MiB scratch instead of a caller workspace.
+
+    For callers that may not allocate device memory when they call the decode.
+    Calls share the scratch: order them on one stream.
+    """
+    batch, num_qo_heads, head_dim = q.shape
+    num_total_pages, num_kv_heads, page_size, _ = k_data.shape
+    _check(_lib.pd_paged_decode_noalloc(
+        _ptr(q), _ptr(k_data), _ptr(v_data), _ptr(indices) if indices.numel() else None, _ptr(indptr),
+        _ptr(last_page_len), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+        num_total_pages, indices.numel(), float(sm_scale), _dtype_code(q), _stream(stream)))
 
 
 def pd_paged_append(k_new, v_new, k_data, v_data, indices, indptr, last_page_len, workspace,

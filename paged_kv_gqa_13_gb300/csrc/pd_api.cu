@@ -542,3 +542,66 @@ pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- decode with built-in scratch
+//
+// Some callers cannot allocate device memory when they call the decode: an
+// engine plugin whose host framework owns every device buffer and hands the
+// op no scratch, or a serving loop that bans cudaMalloc on its hot path
+// because it can synchronize the device and fragment the memory pool. For
+// them pd_paged_decode_noalloc runs the same decode with its scratch in the
+// fixed-size array below, which every device that loads this library keeps
+// for the life of the process.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+std::vector<void*> g_noalloc_addr;  // device address of the array, per device ordinal
+
+// The host-side name of a __device__ array is not its device address; ask the
+// runtime for it once per device, with that device current.
+pd_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (int(g_noalloc_addr.size()) <= dev) g_noalloc_addr.resize(dev + 1, nullptr);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return PD_OK;
+}
+
+}  // namespace
+
+extern "C" pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, const void* v_data,
+                                             const int32_t* indices, const int32_t* indptr,
+                                             const int32_t* last_page_len, void* o, float* lse, int batch,
+                                             int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                                             int num_total_pages, int num_indices, float sm_scale, pd_dtype dtype,
+                                             void* stream) {
+    void* scratch = nullptr;
+    pd_status st = noalloc_scratch(&scratch);
+    if (st != PD_OK) return st;
+    Plan pl;
+    if ((st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl)) != PD_OK) return st;
+    if (pl.ws_bytes > kNoAllocScratchBytes)
+        return fail(PD_ERR_WORKSPACE,
+                    "this shape needs %zu bytes of decode scratch; pd_paged_decode_noalloc has %zu "
+                    "(use pd_paged_decode with a caller workspace)",
+                    pl.ws_bytes, kNoAllocScratchBytes);
+    // The array keeps the last call's contents; the status word must start at zero.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, PD_WORKSPACE_HEADER_BYTES, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch header");
+    return pd_paged_decode(q, k_data, v_data, indices, indptr, last_page_len, o, lse, batch, num_qo_heads,
+                           num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale, dtype,
+                           scratch, kNoAllocScratchBytes, stream);
+}
