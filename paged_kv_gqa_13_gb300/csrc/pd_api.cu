@@ -7,8 +7,11 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "../../include/pagedecode.h"
-#include "pd_decode.cuh"
+#include "pd_kernels.cuh"
 
 namespace pd {
 bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks);
@@ -132,10 +135,10 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
     pd_status st = device_info(&di);
     if (st != PD_OK) return st;
     p->table_bytes = pd::table_bytes_for(!contiguous && batch <= pd::kTableMax);
-    p->nwarps = (di.max_smem - p->table_bytes) / p->ks.warp_bytes;
+    p->nwarps = (di.max_smem - p->table_bytes - p->ks.smem_slack) / p->ks.warp_bytes;
     if (p->nwarps > 8) p->nwarps = 8;
     if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
-    p->smem = size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
+    p->smem = size_t(p->ks.smem_slack) + size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
     if ((st = allow_smem(p->ks.decode, int(p->smem))) != PD_OK) return st;
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->ks.decode, p->nwarps * 32, p->smem);
@@ -148,6 +151,44 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
     p->ws_bytes = p->o_off + size_t(p->slots) * p->G * D * 4;
+    return PD_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+// The driver's tensor-map encoder, reached through the runtime so that the
+// library needs no link against the driver library.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// K or V as a 4-D tensor {head_dim, slab_rows, kv heads, slabs} of 16-bit
+// elements, read in boxes of 64 columns x 16 rows with the 128-byte swizzle;
+// rows outside the tensor read as zero.
+pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long slab_rows, int Hk,
+                      long long slabs) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(slab_rows), cuuint64_t(Hk), cuuint64_t(slabs)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(slab_rows) * D * 2,
+                                   cuuint64_t(Hk) * slab_rows * D * 2};
+    const cuuint32_t box[4] = {64, cuuint32_t(pd::kMmaRows), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, dt == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return PD_OK;
 }
 
@@ -183,7 +224,13 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 
 // ---------------------------------------------------------------- decode launch
 
-pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, cudaStream_t stream) {
+pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, cudaStream_t stream) {
+    CUtensorMap maps[2];
+    if (pl.ks.tensor_maps && a.total_pos > 0) {
+        pd_status st = make_kv_map(&maps[0], a.k, dt, D, a.slab_rows, a.num_kv_heads, slabs);
+        if (st == PD_OK) st = make_kv_map(&maps[1], a.v, dt, D, a.slab_rows, a.num_kv_heads, slabs);
+        if (st != PD_OK) return st;
+    }
     std::unique_lock<std::mutex> plk(g_prof_mu);
     const bool prof = g_prof.on;
     if (!prof) plk.unlock();
@@ -197,7 +244,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, cudaStream_t s
         cfg.blockDim = dim3(pl.nwarps * 32);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = stream;
-        void* args[] = {&a};
+        void* args[] = {&a, &maps[0], &maps[1]};
         if (prof) mark(&g_prof.decode_marks, stream);
         e = cudaLaunchKernelExC(&cfg, pl.ks.decode, args);
         if (prof) mark(&g_prof.decode_marks, stream);
@@ -238,7 +285,6 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, cudaStream_t s
     e = cudaLaunchKernelExC(&cfg, pl.ks.merge, margs);
     if (prof) mark(&g_prof.merge_marks, stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    (void)D;
     return ok();
 }
 
@@ -371,7 +417,8 @@ pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data,
     a.total_pos = (long long)pl.head_tiles * num_kv_heads * num_indices;
     a.q_scale = sm_scale * pd::kLog2e;
     a.contiguous = 0;
-    return launch_decode(pl, a, head_dim, static_cast<cudaStream_t>(stream));
+    a.slab_rows = page_size;
+    return launch_decode(pl, a, head_dim, dtype, num_total_pages, static_cast<cudaStream_t>(stream));
 }
 
 pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int batch,
@@ -422,11 +469,11 @@ pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v
     a.total_pos = (long long)pl.head_tiles * num_kv_heads * n_pos;
     a.q_scale = sm_scale * pd::kLog2e;
     a.contiguous = 1;
-    a.max_kv_len = max_kv_len;
+    a.slab_rows = max_kv_len;
     a.valid_kv_len = valid_kv_len;
     a.vpage = vpage;
     a.npv = npv;
-    return launch_decode(pl, a, head_dim, static_cast<cudaStream_t>(stream));
+    return launch_decode(pl, a, head_dim, dtype, batch, static_cast<cudaStream_t>(stream));
 }
 
 pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, void* v_data, const int32_t* indices,

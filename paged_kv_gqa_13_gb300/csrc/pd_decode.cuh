@@ -1,53 +1,41 @@
-// Batched decode attention over a paged (or contiguous) KV cache: the decode
-// kernel and the kernel that merges its split results.
+// Batched decode attention over a paged (or contiguous) KV cache on CUDA
+// cores: the kernel for groups of up to 4 q heads per kv head, and for f32.
 //
-// Work decomposition. One "position" is one (kv head, head tile, listed page)
-// triple; a pass over all listed pages is made for every (kv head, head tile).
-// All positions of the call, total_pos = head_tiles * num_kv_heads * n_pos,
-// are cut into equal contiguous ranges, one per warp of a grid sized to fill
-// every SM. A warp therefore streams ~total_pos/warps pages regardless of how
-// the lengths are spread over requests: a long request is split over several
-// warps (split-KV), many short ones share a warp. Where a warp's range covers
-// a request's whole page list the warp writes o and lse itself; otherwise it
-// writes a normalised partial (o, lse) into the workspace slot (warp + segment),
-// and merge_partials_kernel combines the partials in warp order.
+// Work decomposition (see pd_walk.cuh). All positions of the call are cut into
+// equal contiguous ranges, one per warp of a grid that fills every SM. A warp
+// therefore streams ~total_pos/warps page slices whatever the length mix: a
+// long request is split over several warps (split-KV), many short ones share
+// a warp. Where a warp's range covers a request's whole page list the warp
+// writes o and lse itself; otherwise it writes a normalised partial (o, lse)
+// into workspace slot (warp + segment), and merge_partials_kernel combines
+// the partials in warp order.
 //
 // Inside a warp. The warp runs its own kStages-deep ring in shared memory.
-// Lane 0 issues 1-D bulk async copies (cp.async.bulk) of whole K and V page
-// slices -- in the HND layout rows [r0, r1) of one (page, kv head) are one
+// Lane 0 issues 1-D bulk async copies (cp.async.bulk) of K and V page slices
+// -- in the HND layout rows [r0, r1) of one (page, kv head) are one
 // contiguous block -- plus, at the start of a request, the group's q rows.
-// Completion is counted in bytes on the stage's mbarrier. While stage s is
-// being consumed, the next stages are in flight.
+// Completion is counted in bytes on the stage's mbarrier. While one stage is
+// being consumed, the next ones are in flight.
 //
-// Arithmetic (CUDA cores, f32). Lane (row group rg, column c) holds EPL
-// elements of the head dimension for every q head of the group. For a round
-// of RR rows it forms the group's partial dot products for those rows, then a
-// reduce-scatter over the L lanes of the row group leaves each lane with a
-// few complete scores. Softmax runs in log2 units (q is pre-scaled by
-// sm_scale*log2 e) against a per-head reference maximum m that only moves
-// when a score exceeds it by more than kTau; a move rescales the
+// Arithmetic (f32). Lane (row group rg, column c) holds EPL elements of the
+// head dimension for every q head of the group. For a round of RR rows it
+// forms the group's partial dot products for those rows with packed f32x2
+// FMAs, then a reduce-scatter over the L lanes of the row group leaves each
+// lane with a few complete scores. Softmax runs in log2 units (q is
+// pre-scaled by sm_scale*log2 e) against a per-head reference maximum m that
+// only moves when a score exceeds it by more than kTau; a move rescales the
 // accumulators. P is broadcast through shared memory and every lane adds
 // p * v into its accumulators for its columns. K and V bytes are read from
 // HBM once for the whole group.
 #pragma once
 
-#include "pd_device.cuh"
+#include "pd_walk.cuh"
 
 namespace pd {
 
 constexpr int kStages = 3;
 constexpr int kChunkBytes = 4096;  // K bytes of one stage (V the same)
-constexpr int kTableMax = 512;     // requests whose indptr / last_page_len are staged in smem
 constexpr float kTau = 8.0f;       // reference max slack, log2 units: p <= 2^kTau
-
-// Chunk metadata flags.
-constexpr int kSegStart = 1, kSegEnd = 2, kSegComplete = 4, kEndOfWork = 8;
-
-__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
-
-inline constexpr int table_bytes_for(bool staged) {
-    return staged ? round_up((2 * kTableMax + 1) * 4, 128) : 0;
-}
 
 template <typename T, int D, int G>
 struct Cfg {
@@ -83,11 +71,10 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     constexpr int kVec = C::kVec, kNvec = C::kNvec, kEpl = C::kEpl, kRC = C::kRC;
     const float kNegInf = -__int_as_float(0x7f800000);
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const bool contiguous = a.contiguous != 0;
     const bool staged = a.table_bytes > 0;
     int* s_indptr = reinterpret_cast<int*>(smem);
     int* s_lpl = s_indptr + kTableMax + 1;
@@ -95,6 +82,15 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     int4* meta = reinterpret_cast<int4*>(wsm + C::kMetaOff);
     const uint32_t bar0 = smem_u32(wsm + C::kBarOff);
     float* pbuf = reinterpret_cast<float*>(wsm + C::kPbufOff);
+
+    // This warp's range of positions; the page ids of its first two windows
+    // are requested before the set-up so that their latency overlaps it.
+    const long long gwarp = (long long)blockIdx.x * nwarps + wid;
+    const long long p0 = gwarp * a.pos_per_warp;
+    const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
+    Walk walk(a, s_indptr, s_lpl, p0, pend, lane);
+    const int first_page = walk.prefetch_first();
+    const int GT = a.heads_per_tile;
 
     // ---- set-up: stage the page table, zero the ring, init the barriers
     if (staged) {
@@ -111,162 +107,44 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         fence_mbar_init();
     }
     __syncthreads();  // the only block-wide barrier: warps are independent from here on
+    // Let the merge kernel be scheduled now; it waits for this grid before it
+    // reads any partial result.
+    launch_dependents();
+    if (p0 >= pend) return;
+    walk.build(p0, first_page);
 
-    const long long gwarp = (long long)blockIdx.x * nwarps + wid;
-    const long long p0 = gwarp * a.pos_per_warp;
-    const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
-    if (p0 >= pend) {
-        launch_dependents();
-        return;
-    }
-
-    const int B = a.batch, N = a.n_pos, P = a.page_size, Hk = a.num_kv_heads;
-    const int HT = a.head_tiles, GT = a.heads_per_tile;
-    auto indptr_at = [&](int b) -> int { return staged ? s_indptr[b] : __ldg(a.indptr + b); };
-    auto range_of = [&](int b, int* lo, int* hi) {
-        if (contiguous)
-            request_range(b, N, true, a.npv, 0, 0, lo, hi);
-        else
-            request_range(b, N, false, 0, indptr_at(b), indptr_at(b + 1), lo, hi);
-    };
-    auto last_len = [&](int b) -> int {
-        if (contiguous) return a.valid_kv_len - (a.npv - 1) * a.vpage;
-        int v = staged ? s_lpl[b] : __ldg(a.last_page_len + b);
-        if (v < 0 || v > P) {
-            if (lane == 0) atomicOr(a.flags, kFlagBadLastPageLen);
-            v = v < 0 ? 0 : P;
-        }
-        return v;
-    };
-    // First request whose range ends after position i (B if none).
-    auto find_request = [&](int i) -> int {
-        if (contiguous) return min(i / a.npv, B);
-        int lo = 0, hi = B;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (indptr_at(mid + 1) > i) hi = mid;
-            else lo = mid + 1;
-        }
-        return lo;
-    };
-
-    // ---- producer walk state (identical in every lane)
-    long long wp = p0;  // next position to emit
-    int wsh = int(p0 / N), wi = int(p0 % N);
-    int wb = find_request(wi), wlo = 0, whi = 0, wj = 0;
-    if (wb < B) range_of(wb, &wlo, &whi);
-    bool wfirst = true;
-    // Window of 64 page ids: win0 = indices[wbase + lane], win1 = indices[wbase + 32 + lane].
-    int wbase = -64, win0 = -1, win1 = -1;
-    auto idx_load = [&](int x) -> int { return (x >= 0 && x < N) ? __ldg(a.indices + x) : -1; };
-    auto page_id = [&](int i) -> int {
-        if (i < wbase || i >= wbase + 64) {
-            wbase = i & ~31;
-            win0 = idx_load(wbase + lane);
-            win1 = idx_load(wbase + 32 + lane);
-        } else if (i >= wbase + 32) {
-            wbase += 32;
-            win0 = win1;
-            win1 = idx_load(wbase + 32 + lane);
-        }
-        return __shfl_sync(kFull, win0, i - wbase);
-    };
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(C::kRowBytes);
-
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot) {
-        while (wp < pend) {
-            if (wb >= B) {  // past the last request of this pass: next pass
-                wp += N - wi;
-                ++wsh;
-                wi = 0;
-                wj = 0;
-                wb = find_request(0);
-                if (wb < B) range_of(wb, &wlo, &whi);
-                continue;
-            }
-            if (wi >= whi) {
-                ++wb;
-                if (wb < B) range_of(wb, &wlo, &whi);
-                continue;
-            }
-            if (wi < wlo) {  // positions before this request belong to none
-                wp += wlo - wi;
-                wi = wlo;
-                wj = 0;
-                continue;
-            }
-            break;
-        }
+        Chunk ck;
+        const bool have = walk.next<kRC>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
-        if (wp >= pend) {
-            if (lane == 0) {
-                meta[slot] = make_int4(0, kEndOfWork, 0, 0);
-                mbar_arrive(bar);
-            }
+        if (lane != 0) return;
+        if (!have) {
+            meta[slot] = make_int4(0, kEndOfWork, 0, 0);
+            mbar_arrive(bar);
             return;
         }
-        const int kh = wsh / HT, ht = wsh % HT;
-        int valid, page;
-        size_t src_row;  // element row index of the page slice's row 0
-        if (contiguous) {
-            page = wi - wlo;
-            valid = (wi == whi - 1) ? last_len(wb) : a.vpage;
-            src_row = (size_t(wb) * Hk + kh) * size_t(a.max_kv_len) + size_t(page) * a.vpage;
-        } else {
-            page = page_id(wi);
-            valid = (wi == whi - 1) ? last_len(wb) : P;
-            if (page < 0 || page >= a.num_total_pages) {
-                if (lane == 0) atomicOr(a.flags, kFlagBadPage);
-                valid = 0;
-                page = 0;
-            }
-            src_row = (size_t(page) * Hk + kh) * size_t(P);
+        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
+        const uint32_t kv_bytes = uint32_t(ck.rows) * uint32_t(row_bytes);
+        const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
+        const uint32_t total = 2 * kv_bytes + q_bytes;
+        if (total == 0) {
+            mbar_arrive(bar);
+            return;
         }
-        const int nck = valid > kRC ? (valid + kRC - 1) / kRC : 1;
-        int rows = valid - wj * kRC;
-        rows = rows < 0 ? 0 : (rows > kRC ? kRC : rows);
-        int flags = 0;
-        if (wfirst || (wi == wlo && wj == 0)) flags |= kSegStart;
-        if (wj == nck - 1 && (wi == whi - 1 || wp + 1 == pend)) flags |= kSegEnd;
-        const long long seg_lo = (long long)wsh * N + wlo, seg_hi = (long long)wsh * N + whi;
-        if (seg_lo >= p0 && seg_hi <= pend) flags |= kSegComplete;
-        if (lane == 0) {
-            meta[slot] = make_int4(rows, flags, wb, wsh);
-            const uint32_t kv_bytes = uint32_t(rows) * uint32_t(row_bytes);
-            const uint32_t q_bytes = (flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
-            const uint32_t total = 2 * kv_bytes + q_bytes;
-            if (total == 0) {
-                mbar_arrive(bar);
-            } else {
-                mbar_arrive_expect_tx(bar, total);
-                if (kv_bytes) {
-                    const size_t off = (src_row + size_t(wj) * kRC) * row_bytes;
-                    bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
-                    bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes,
-                             bar, policy);
-                }
-                if (q_bytes) {
-                    const size_t qoff = (size_t(wb) * a.num_qo_heads + size_t(kh) * a.group +
-                                         size_t(ht) * GT) * row_bytes;
-                    bulk_g2s(smem_u32(st + 2 * kChunkBytes), static_cast<const uint8_t*>(a.q) + qoff, q_bytes,
-                             bar);
-                }
-            }
+        mbar_arrive_expect_tx(bar, total);
+        if (kv_bytes) {
+            const size_t off =
+                ((size_t(ck.slab) * a.num_kv_heads + ck.kh) * size_t(a.slab_rows) + size_t(ck.row0)) * row_bytes;
+            bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
+            bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar, policy);
         }
-        wfirst = false;
-        if (++wj == nck) {
-            wj = 0;
-            ++wp;
-            if (++wi == N) {
-                ++wsh;
-                wi = 0;
-                wb = find_request(0);
-                if (wb < B) range_of(wb, &wlo, &whi);
-            }
-        }
+        if (q_bytes)
+            bulk_g2s(smem_u32(st + 2 * kChunkBytes), static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes,
+                     q_bytes, bar);
     };
 
     // ---- consumer state
@@ -284,8 +162,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     // one value; only the first lane of each group counts it into the sum.
     const bool primary = (kV >= kL) || ((c & ((kL >= kV ? kL / kV : 1) - 1)) == 0);
 
-    float qf[G][kEpl];
-    float acc[G][kEpl];
+    // q and the accumulators are kept as float2 pairs of adjacent columns so
+    // that the dot products and the P.V update use packed f32x2 FMAs.
+    constexpr int kEp2 = kEpl / 2;
+    float2 qf[G][kEp2];
+    float2 acc[G][kEp2];
     float mref[G];
     float mmy[kVF], lmy[kVF];
     auto reset_state = [&]() {
@@ -293,7 +174,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         for (int h = 0; h < G; ++h) {
             mref[h] = kNegInf;
 #pragma unroll
-            for (int e = 0; e < kEpl; ++e) acc[h][e] = 0.f;
+            for (int e = 0; e < kEp2; ++e) acc[h][e] = make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int j = 0; j < kVF; ++j) mmy[j] = kNegInf, lmy[j] = 0.f;
@@ -320,32 +201,36 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int e = 0; e < kEpl; ++e) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], off);
-        const int b = m.z, sh = m.w;
-        const int kh = sh / HT, ht = sh % HT;
-        const int head0 = kh * a.group + ht * GT;
+                for (int e = 0; e < kEp2; ++e) {
+                    acc[h][e].x += __shfl_xor_sync(kFull, acc[h][e].x, off);
+                    acc[h][e].y += __shfl_xor_sync(kFull, acc[h][e].y, off);
+                }
+        const int qrow = m.z;  // first q / o row of the group
         if (m.y & kSegComplete) {
             if (lane < kL) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     if (h >= GT) break;
                     const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
-                    T* orow = static_cast<T*>(a.o) + (size_t(b) * a.num_qo_heads + head0 + h) * D;
+                    T* orow = static_cast<T*>(a.o) + (size_t(qrow) + h) * D;
 #pragma unroll
                     for (int nv = 0; nv < kNvec; ++nv) {
                         float f[kVec];
 #pragma unroll
-                        for (int e = 0; e < kVec; ++e) f[e] = acc[h][nv * kVec + e] * inv;
+                        for (int e = 0; e < kVec / 2; ++e) {
+                            f[2 * e] = acc[h][nv * kVec / 2 + e].x * inv;
+                            f[2 * e + 1] = acc[h][nv * kVec / 2 + e].y * inv;
+                        }
                         *reinterpret_cast<uint4*>(orow + (nv * kL + c) * kVec) = E::from_f32(f);
                     }
                 }
             }
             if (a.lse != nullptr && lane < GT) {
                 const float l = pick(lh, lane), mr = pick(mref, lane);
-                a.lse[size_t(b) * a.num_qo_heads + head0 + lane] = l > 0.f ? (mr + log2f(l)) * kLn2 : kNegInf;
+                a.lse[size_t(qrow) + lane] = l > 0.f ? (mr + log2f(l)) * kLn2 : kNegInf;
             }
         } else {
-            const long long slot = gwarp + (long long)sh * B + b;
+            const long long slot = gwarp + m.w;
             if (lane < kL) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -355,10 +240,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
 #pragma unroll
                     for (int nv = 0; nv < kNvec; ++nv)
 #pragma unroll
-                        for (int e4 = 0; e4 < kVec; e4 += 4)
-                            *reinterpret_cast<float4*>(prow + (nv * kL + c) * kVec + e4) =
-                                make_float4(acc[h][nv * kVec + e4] * inv, acc[h][nv * kVec + e4 + 1] * inv,
-                                            acc[h][nv * kVec + e4 + 2] * inv, acc[h][nv * kVec + e4 + 3] * inv);
+                        for (int e4 = 0; e4 < kVec / 2; e4 += 2) {
+                            const float2 u = acc[h][nv * kVec / 2 + e4], w2 = acc[h][nv * kVec / 2 + e4 + 1];
+                            *reinterpret_cast<float4*>(prow + (nv * kL + c) * kVec + 2 * e4) =
+                                make_float4(u.x * inv, u.y * inv, w2.x * inv, w2.y * inv);
+                        }
                 }
             }
             if (lane < GT) {
@@ -386,7 +272,8 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
                         for (int e = 0; e < kVec; ++e) f[e] = 0.f;
                     }
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e) qf[h][nv * kVec + e] = f[e] * a.q_scale;
+                    for (int e = 0; e < kVec / 2; ++e)
+                        qf[h][nv * kVec / 2 + e] = make_float2(f[2 * e] * a.q_scale, f[2 * e + 1] * a.q_scale);
                 }
         }
         const int rows = m.x;
@@ -394,10 +281,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         for (int rd = 0; rd < C::kRounds; ++rd) {
             const int r0 = rd * kRW * kRR;
             if (r0 >= rows) break;
-            // scores: partial dot products of this lane's columns
-            float part[kV];
+            // scores: partial dot products of this lane's columns, even and odd
+            // columns in the two halves of a float2
+            float2 part2[kV];
 #pragma unroll
-            for (int x = 0; x < kV; ++x) part[x] = 0.f;
+            for (int x = 0; x < kV; ++x) part2[x] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int rr = 0; rr < kRR; ++rr) {
                 const int r = r0 + rr * kRW + rg;
@@ -408,10 +296,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
-                        for (int e = 0; e < kVec; ++e)
-                            part[rr * G + h] = fmaf(qf[h][nv * kVec + e], f[e], part[rr * G + h]);
+                        for (int e = 0; e < kVec / 2; ++e)
+                            part2[rr * G + h] = __ffma2_rn(qf[h][nv * kVec / 2 + e],
+                                                           make_float2(f[2 * e], f[2 * e + 1]), part2[rr * G + h]);
                 }
             }
+            float part[kV];
+#pragma unroll
+            for (int x = 0; x < kV; ++x) part[x] = part2[x].x + part2[x].y;
             RS::run(part, lane);
             // softmax against the reference max
             float x[kVF];
@@ -433,8 +325,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
                     const float mn = fmaxf(mref[h], mh);
                     alpha[h] = (mn == kNegInf) ? 1.f : ex2(mref[h] - mn);
                     mref[h] = mn;
+                    const float2 al2 = make_float2(alpha[h], alpha[h]);
 #pragma unroll
-                    for (int e = 0; e < kEpl; ++e) acc[h][e] *= alpha[h];
+                    for (int e = 0; e < kEp2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], al2);
                 }
 #pragma unroll
                 for (int j = 0; j < kVF; ++j) {
@@ -473,10 +366,13 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
                     float f[kVec];
                     E::to_f32(*reinterpret_cast<const uint4*>(vb + r * C::kRowBytes + (nv * kL + c) * 16), f);
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
+                    for (int h = 0; h < G; ++h) {
+                        const float2 p2 = make_float2(pv[rr * G + h], pv[rr * G + h]);
 #pragma unroll
-                        for (int e = 0; e < kVec; ++e)
-                            acc[h][nv * kVec + e] = fmaf(pv[rr * G + h], f[e], acc[h][nv * kVec + e]);
+                        for (int e = 0; e < kVec / 2; ++e)
+                            acc[h][nv * kVec / 2 + e] =
+                                __ffma2_rn(p2, make_float2(f[2 * e], f[2 * e + 1]), acc[h][nv * kVec / 2 + e]);
+                    }
                 }
             }
         }
@@ -505,154 +401,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         __syncwarp();
         produce(slot);
     }
-    launch_dependents();
 }
 
-// One warp per (request, kv head, head tile, q head): combine the partial
-// results the decode warps wrote for a request split across warps, in warp
-// order; write zeros / -inf for requests with no pages.
-template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_partials_kernel(const MergeArgs a) {
-    constexpr int kPer = D / 32;  // elements per lane
-    const float kNegInf = -__int_as_float(0x7f800000);
-    grid_dependency_wait();  // the decode kernel's partials are complete and visible
-    const int lane = threadIdx.x & 31;
-    const long long pair = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const long long segments = (long long)a.head_tiles * a.num_kv_heads * a.batch;
-    if (pair >= segments * a.heads_per_tile) return;
-    const int h = int(pair % a.heads_per_tile);
-    const long long s = pair / a.heads_per_tile;
-    const int b = int(s % a.batch), sh = int(s / a.batch);
-    const int kh = sh / a.head_tiles, ht = sh % a.head_tiles;
-    const int head = kh * a.group + ht * a.heads_per_tile + h;
-    int lo, hi;
-    if (a.contiguous) {
-        request_range(b, a.n_pos, true, a.npv, 0, 0, &lo, &hi);
-    } else {
-        const int r0 = __ldg(a.indptr + b), r1 = __ldg(a.indptr + b + 1);
-        if (sh == 0 && h == 0 && lane == 0 && (r0 < 0 || r1 < r0 || r1 > a.n_pos))
-            atomicOr(a.flags, kFlagBadIndptr);
-        request_range(b, a.n_pos, false, 0, r0, r1, &lo, &hi);
-    }
-    T* orow = static_cast<T*>(a.o) + (size_t(b) * a.num_qo_heads + head) * D;
-    float* lse_out = a.lse ? a.lse + size_t(b) * a.num_qo_heads + head : nullptr;
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float L = kNegInf;
-    if (hi > lo) {
-        const long long first = ((long long)sh * a.n_pos + lo) / a.pos_per_warp;
-        const long long last = ((long long)sh * a.n_pos + hi - 1) / a.pos_per_warp;
-        if (first == last) return;  // one warp held the whole request and wrote it
-        const int parts = int(last - first + 1);
-        auto slot_of = [&](int cpart) { return (first + cpart + s) * a.G + h; };
-        float M = kNegInf;
-        for (int cp = lane; cp < parts; cp += 32) M = fmaxf(M, a.part_lse[slot_of(cp)]);
-        M = warp_max(M);
-        if (M != kNegInf) {
-            float S = 0.f;
-            for (int cp = lane; cp < parts; cp += 32) S += ex2(a.part_lse[slot_of(cp)] - M);
-            S = warp_sum(S);
-            L = M + log2f(S);
-            for (int cp = 0; cp < parts; ++cp) {
-                const long long sl = slot_of(cp);
-                const float w = ex2(a.part_lse[sl] - L);
-                const float* po = a.part_o + size_t(sl) * D + lane * kPer;
-#pragma unroll
-                for (int e = 0; e < kPer; e += 2) {
-                    const float2 t = *reinterpret_cast<const float2*>(po + e);
-                    acc[e] = fmaf(w, t.x, acc[e]);
-                    acc[e + 1] = fmaf(w, t.y, acc[e + 1]);
-                }
-            }
-        }
-    }
-    // Each lane writes its kPer consecutive elements.
-    if constexpr (sizeof(T) == 4) {
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2)
-            *reinterpret_cast<float2*>(reinterpret_cast<float*>(orow) + lane * kPer + e) = make_float2(acc[e], acc[e + 1]);
-    } else {
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-            const uint32_t w = Elt<T>::pack(acc[e], acc[e + 1]);
-            *reinterpret_cast<uint32_t*>(orow + lane * kPer + e) = w;
-        }
-    }
-    if (lse_out && lane == 0) *lse_out = (L == kNegInf) ? kNegInf : L * kLn2;
-}
-
-// Standalone merge of caller-supplied parts (natural-log lse), one warp per row.
-template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_states_kernel(const float* o_parts, const float* lse_parts,
-                                                            int num_parts, int num_rows, void* o, float* lse) {
-    constexpr int kPer = D / 32;
-    const float kNegInf = -__int_as_float(0x7f800000);
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= num_rows) return;
-    auto lse2 = [&](int cp) { return lse_parts[size_t(cp) * num_rows + row] * kLog2e; };
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float M = kNegInf;
-    for (int cp = lane; cp < num_parts; cp += 32) M = fmaxf(M, lse2(cp));
-    M = warp_max(M);
-    float L = kNegInf;
-    if (M != kNegInf) {
-        float S = 0.f;
-        for (int cp = lane; cp < num_parts; cp += 32) S += ex2(lse2(cp) - M);
-        S = warp_sum(S);
-        L = M + log2f(S);
-        for (int cp = 0; cp < num_parts; ++cp) {
-            const float w = ex2(lse2(cp) - L);
-            const float* po = o_parts + (size_t(cp) * num_rows + row) * D + lane * kPer;
-#pragma unroll
-            for (int e = 0; e < kPer; e += 2) {
-                const float2 t = *reinterpret_cast<const float2*>(po + e);
-                acc[e] = fmaf(w, t.x, acc[e]);
-                acc[e + 1] = fmaf(w, t.y, acc[e + 1]);
-            }
-        }
-    }
-    T* orow = static_cast<T*>(o) + size_t(row) * D;
-    if constexpr (sizeof(T) == 4) {
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2)
-            *reinterpret_cast<float2*>(reinterpret_cast<float*>(orow) + lane * kPer + e) = make_float2(acc[e], acc[e + 1]);
-    } else {
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2)
-            *reinterpret_cast<uint32_t*>(orow + lane * kPer + e) = Elt<T>::pack(acc[e], acc[e + 1]);
-    }
-    if (lse && lane == 0) lse[row] = (L == kNegInf) ? kNegInf : L * kLn2;
-}
-
-// Kernels and sizes for one (T, D, G) combination, handed to the host code.
-struct KernelSet {
-    const void* decode;
-    const void* merge;
-    const void* merge_states;
-    int warp_bytes;      // dynamic shared memory per decode warp
-    int rows_per_stage;  // K (and V) rows one pipeline stage holds
-};
-
-template <typename T>
-bool lookup_kernels_t(int D, int G, KernelSet* ks) {
-#define PD_CASE(DD, GG)                                                        \
-    if (D == DD && G == GG) {                                                  \
-        ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG>);  \
-        ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>); \
-        ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>); \
-        ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                           \
-        ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                              \
-        return true;                                                           \
-    }
-    PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)
-    PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)
-    PD_CASE(256, 1) PD_CASE(256, 2) PD_CASE(256, 4) PD_CASE(256, 8)
-#undef PD_CASE
-    return false;
-}
 
 }  // namespace pd

@@ -1,0 +1,52 @@
+// The kernel variants for one element type, looked up by the host code.
+#pragma once
+
+#include <type_traits>
+
+#include "pd_decode.cuh"
+#include "pd_decode_mma.cuh"
+#include "pd_merge.cuh"
+
+namespace pd {
+
+// Kernels and sizes for one (T, head_dim, heads per tile) combination.
+struct KernelSet {
+    const void* decode;
+    const void* merge;
+    const void* merge_states;
+    int warp_bytes;      // dynamic shared memory per decode warp
+    int rows_per_stage;  // K (and V) rows one pipeline stage holds
+    int tensor_maps;     // 1: the decode kernel takes K and V tensor maps (tensor-core kernel)
+    int smem_slack;      // extra dynamic shared memory for aligning the stages
+};
+
+template <typename T>
+bool lookup_kernels_t(int D, int G, KernelSet* ks) {
+    constexpr bool kHalf = sizeof(T) == 2;
+#define PD_CASE(DD, GG)                                                                 \
+    if (D == DD && G == GG) {                                                           \
+        ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>);        \
+        ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>);   \
+        if constexpr (kHalf && GG == 8) {                                               \
+            ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD>);       \
+            ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                 \
+            ks->rows_per_stage = kMmaRows;                                              \
+            ks->tensor_maps = 1;                                                        \
+            ks->smem_slack = 1024;                                                      \
+        } else {                                                                        \
+            ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG>);       \
+            ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
+            ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                   \
+            ks->tensor_maps = 0;                                                        \
+            ks->smem_slack = 0;                                                         \
+        }                                                                               \
+        return true;                                                                    \
+    }
+    PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)
+    PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)
+    PD_CASE(256, 1) PD_CASE(256, 2) PD_CASE(256, 4) PD_CASE(256, 8)
+#undef PD_CASE
+    return false;
+}
+
+}  // namespace pd

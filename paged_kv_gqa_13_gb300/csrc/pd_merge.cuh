@@ -1,0 +1,123 @@
+// Merge of split attention states: the kernel that combines the decode's
+// partial (o, lse) results, and the standalone merge of caller-supplied parts.
+#pragma once
+
+#include "pd_walk.cuh"
+
+namespace pd {
+
+// Weighted sum of partial rows, parts taken in index order: lane c of each
+// group of 32 parts computes its part's weight 2^(lse_c - L); the weights are
+// broadcast with shuffles and every lane accumulates its kPer columns.
+template <int kPer, class LseAt, class RowAt>
+__device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_at, float* acc) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    const int lane = threadIdx.x & 31;
+    float M = kNegInf;
+    for (int cp = lane; cp < parts; cp += 32) M = fmaxf(M, lse_at(cp));
+    M = warp_max(M);
+    if (M == kNegInf) return kNegInf;
+    float S = 0.f;
+    for (int cp = lane; cp < parts; cp += 32) S += ex2(lse_at(cp) - M);
+    S = warp_sum(S);
+    const float L = M + log2f(S);
+    for (int base = 0; base < parts; base += 32) {
+        const int n = min(32, parts - base);
+        const float w_mine = (lane < n) ? ex2(lse_at(base + lane) - L) : 0.f;
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float w = __shfl_sync(kFull, w_mine, j);
+            const float* po = row_at(base + j) + lane * kPer;
+#pragma unroll
+            for (int e = 0; e < kPer; e += 2) {
+                const float2 t = *reinterpret_cast<const float2*>(po + e);
+                acc[e] = fmaf(w, t.x, acc[e]);
+                acc[e + 1] = fmaf(w, t.y, acc[e + 1]);
+            }
+        }
+    }
+    return L;
+}
+
+template <typename T, int kPer>
+__device__ __forceinline__ void store_row(T* orow, const float* acc) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2)
+            *reinterpret_cast<float2*>(reinterpret_cast<float*>(orow) + lane * kPer + e) = make_float2(acc[e], acc[e + 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2)
+            *reinterpret_cast<uint32_t*>(orow + lane * kPer + e) = Elt<T>::pack(acc[e], acc[e + 1]);
+    }
+}
+
+// One warp per (request, kv head, head tile, q head): combine the partial
+// results the decode warps wrote for a request split across warps, in warp
+// order; write zeros / -inf for requests with no pages. Everything that does
+// not depend on the decode's output (the page table, empty requests) is done
+// before waiting for the decode grid.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_partials_kernel(const MergeArgs a) {
+    constexpr int kPer = D / 32;  // elements per lane
+    const float kNegInf = -__int_as_float(0x7f800000);
+    const int lane = threadIdx.x & 31;
+    const long long pair = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long segments = (long long)a.head_tiles * a.num_kv_heads * a.batch;
+    if (pair >= segments * a.heads_per_tile) return;
+    const int h = int(pair % a.heads_per_tile);
+    const long long s = pair / a.heads_per_tile;
+    const int b = int(s % a.batch), sh = int(s / a.batch);
+    const int kh = sh / a.head_tiles, ht = sh % a.head_tiles;
+    const int head = kh * a.group + ht * a.heads_per_tile + h;
+    int lo, hi;
+    if (a.contiguous) {
+        request_range(b, a.n_pos, true, a.npv, 0, 0, &lo, &hi);
+    } else {
+        const int r0 = __ldg(a.indptr + b), r1 = __ldg(a.indptr + b + 1);
+        if (sh == 0 && h == 0 && lane == 0 && (r0 < 0 || r1 < r0 || r1 > a.n_pos))
+            atomicOr(a.flags, kFlagBadIndptr);
+        request_range(b, a.n_pos, false, 0, r0, r1, &lo, &hi);
+    }
+    T* orow = static_cast<T*>(a.o) + (size_t(b) * a.num_qo_heads + head) * D;
+    float* lse_out = a.lse ? a.lse + size_t(b) * a.num_qo_heads + head : nullptr;
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float L = kNegInf;
+    if (hi > lo) {
+        const long long first = ((long long)sh * a.n_pos + lo) / a.pos_per_warp;
+        const long long last = ((long long)sh * a.n_pos + hi - 1) / a.pos_per_warp;
+        if (first == last) return;  // one warp held the whole request and wrote it
+        grid_dependency_wait();     // the decode kernel's partials are complete and visible
+        const int parts = int(last - first + 1);
+        const long long slot0 = (first + s) * a.G + h;  // slot of part c: (first + c + s) * G + h
+        L = merge_rows<kPer>(
+            parts, [&](int cp) { return a.part_lse[slot0 + (long long)cp * a.G]; },
+            [&](int cp) { return a.part_o + size_t(slot0 + (long long)cp * a.G) * D; }, acc);
+    }
+    store_row<T, kPer>(orow, acc);
+    if (lse_out && lane == 0) *lse_out = (L == kNegInf) ? kNegInf : L * kLn2;
+}
+
+// Standalone merge of caller-supplied parts (natural-log lse), one warp per row.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_states_kernel(const float* o_parts, const float* lse_parts,
+                                                            int num_parts, int num_rows, void* o, float* lse) {
+    constexpr int kPer = D / 32;
+    const float kNegInf = -__int_as_float(0x7f800000);
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= num_rows) return;
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    const float L = merge_rows<kPer>(
+        num_parts, [&](int cp) { return lse_parts[size_t(cp) * num_rows + row] * kLog2e; },
+        [&](int cp) { return o_parts + (size_t(cp) * num_rows + row) * D; }, acc);
+    store_row<T, kPer>(static_cast<T*>(o) + size_t(row) * D, acc);
+    if (lse && lane == 0) lse[row] = (L == kNegInf) ? kNegInf : L * kLn2;
+}
+
+}  // namespace pd

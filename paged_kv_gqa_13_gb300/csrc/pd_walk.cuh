@@ -1,0 +1,190 @@
+// The walk over one warp's range of positions, shared by the decode kernels.
+//
+// A position is one (kv head, head tile, listed page) triple: the pages of the
+// table are visited once per (kv head, head tile) "pass", in table order, and
+// position p is page p % n_pos of pass p / n_pos. A warp owns the positions
+// [p0, pend). Request b owns, in every pass, the positions
+// [indptr[b], indptr[b+1]) of the table (batch_paged_decode.rs, "Layout":
+// indptr is a prefix sum into indices; the last page holds last_page_len
+// rows). The contiguous cache is walked the same way with each request's rows
+// cut into virtual pages of `vpage` rows.
+//
+// The walk describes 32 positions at a time, one per lane, so that the
+// per-position work (finding the request, reading the page id, the
+// last-page length, the flags) runs in parallel; emitting a chunk then costs a
+// few shuffles. Page ids of the next window are loaded one window ahead.
+#pragma once
+
+#include "pd_device.cuh"
+
+namespace pd {
+
+constexpr int kTableMax = 512;  // requests whose indptr / last_page_len are staged in smem
+
+// Chunk metadata flags.
+constexpr int kSegStart = 1, kSegEnd = 2, kSegComplete = 4, kEndOfWork = 8;
+
+__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+inline constexpr int table_bytes_for(bool staged) {
+    return staged ? round_up((2 * kTableMax + 1) * 4, 1024) : 0;
+}
+
+// One chunk of up to `chunk_rows` rows of one position.
+struct Chunk {
+    int slab;   // outer index of the K/V slab: page id (paged) or request (contiguous)
+    int kh;     // kv head
+    int row0;   // first row of the chunk within the (slab, kv head) rows
+    int rows;   // valid rows in the chunk (0 .. chunk_rows)
+    int flags;  // kSegStart / kSegEnd / kSegComplete
+    int qrow;   // first q / o row of the group: b * num_qo_heads + first head of the tile
+    int seg;    // segment id: pass * batch + b
+};
+
+struct Walk {
+    const DecodeArgs& a;
+    const int* s_indptr;
+    const int* s_lpl;
+    long long p0, pend;
+    int lane;
+    bool contiguous, staged;
+
+    // current window: lane k describes position wbase + k
+    long long wbase;
+    unsigned mask;  // lanes whose position belongs to a request
+    int cur, j;     // lane being emitted, chunk within its position
+    int nxt;        // prefetched page id of position wbase + 32 + lane
+    int e_slab, e_row, e_khf, e_valid, e_qrow, e_seg;  // e_khf = kh << 4 | flags
+
+    __device__ __forceinline__ Walk(const DecodeArgs& args, const int* si, const int* sl, long long p0_,
+                                    long long pend_, int lane_)
+        : a(args), s_indptr(si), s_lpl(sl), p0(p0_), pend(pend_), lane(lane_), contiguous(args.contiguous != 0),
+          staged(args.table_bytes > 0), wbase(p0_), mask(0), cur(0), j(0), nxt(-1),
+          e_slab(0), e_row(0), e_khf(0), e_valid(0), e_qrow(0), e_seg(0) {}
+
+    // Page id of position p (paged store), -1 outside the range.
+    __device__ __forceinline__ int load_page(long long p) const {
+        if (contiguous || p >= pend) return -1;
+        return __ldg(a.indices + int(p % a.n_pos));
+    }
+
+    __device__ __forceinline__ int indptr_at(int b) const { return staged ? s_indptr[b] : __ldg(a.indptr + b); }
+
+    __device__ __forceinline__ void range_of(int b, int* lo, int* hi) const {
+        if (contiguous)
+            request_range(b, a.n_pos, true, a.npv, 0, 0, lo, hi);
+        else
+            request_range(b, a.n_pos, false, 0, indptr_at(b), indptr_at(b + 1), lo, hi);
+    }
+
+    // Valid rows of request b's last page, clamped to [0, page_size] (flagged if outside).
+    __device__ __forceinline__ int last_len(int b) const {
+        if (contiguous) return a.valid_kv_len - (a.npv - 1) * a.vpage;
+        int v = staged ? s_lpl[b] : __ldg(a.last_page_len + b);
+        if (v < 0 || v > a.page_size) {
+            atomicOr(a.flags, kFlagBadLastPageLen);
+            v = v < 0 ? 0 : a.page_size;
+        }
+        return v;
+    }
+
+    // First request whose range ends after position i (batch if none).
+    __device__ __forceinline__ int find_request(int i) const {
+        if (contiguous) return min(i / a.npv, a.batch);
+        int lo = 0, hi = a.batch;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (indptr_at(mid + 1) > i) hi = mid;
+            else lo = mid + 1;
+        }
+        return lo;
+    }
+
+    // Describe positions base .. base + 31, one per lane; pg is this lane's page id.
+    __device__ __forceinline__ void build(long long base, int pg) {
+        const long long p = base + lane;
+        bool has = false;
+        e_slab = 0, e_row = 0, e_khf = 0, e_valid = 0, e_qrow = 0, e_seg = 0;
+        if (p < pend) {
+            const int N = a.n_pos;
+            const int sh = int(p / N), i = int(p % N);
+            const int b = find_request(i);
+            int lo = 0, hi = 0;
+            if (b < a.batch) range_of(b, &lo, &hi);
+            if (b < a.batch && i >= lo && i < hi) {
+                has = true;
+                const int kh = sh / a.head_tiles, ht = sh % a.head_tiles;
+                if (contiguous) {
+                    e_valid = (i == hi - 1) ? last_len(b) : a.vpage;
+                    e_slab = b;
+                    e_row = (i - lo) * a.vpage;
+                } else {
+                    e_valid = (i == hi - 1) ? last_len(b) : a.page_size;
+                    if (pg < 0 || pg >= a.num_total_pages) {
+                        atomicOr(a.flags, kFlagBadPage);
+                        e_valid = 0;
+                        pg = 0;
+                    }
+                    e_slab = pg;
+                }
+                int fl = 0;
+                if (i == lo || p == p0) fl |= kSegStart;
+                if (i == hi - 1 || p == pend - 1) fl |= kSegEnd;
+                if ((long long)sh * N + lo >= p0 && (long long)sh * N + hi <= pend) fl |= kSegComplete;
+                e_khf = (kh << 4) | fl;
+                e_qrow = b * a.num_qo_heads + kh * a.group + ht * a.heads_per_tile;
+                e_seg = sh * a.batch + b;
+            }
+        }
+        mask = __ballot_sync(kFull, has);
+    }
+
+    // Issue the page-id loads of the first two windows (before any other set-up).
+    __device__ __forceinline__ int prefetch_first() {
+        nxt = load_page(p0 + 32 + lane);
+        return load_page(p0 + lane);
+    }
+
+    // The next chunk of at most CR rows; false when the range is exhausted.
+    template <int CR>
+    __device__ __forceinline__ bool next(Chunk* ck) {
+        bool have = false;
+        while (wbase < pend) {
+            const unsigned rest = cur < 32 ? (mask >> cur) : 0u;
+            if (rest != 0u) {
+                cur += __ffs(rest) - 1;
+                have = true;
+                break;
+            }
+            wbase += 32;
+            cur = 0;
+            j = 0;
+            if (wbase >= pend) break;
+            const int pg = nxt;
+            nxt = load_page(wbase + 32 + lane);
+            build(wbase, pg);
+        }
+        if (!have) return false;
+        const int valid = __shfl_sync(kFull, e_valid, cur);
+        const int khf = __shfl_sync(kFull, e_khf, cur);
+        ck->slab = __shfl_sync(kFull, e_slab, cur);
+        ck->row0 = __shfl_sync(kFull, e_row, cur) + j * CR;
+        ck->qrow = __shfl_sync(kFull, e_qrow, cur);
+        ck->seg = __shfl_sync(kFull, e_seg, cur);
+        ck->kh = khf >> 4;
+        const int nck = valid > CR ? (valid + CR - 1) / CR : 1;
+        int rows = valid - j * CR;
+        ck->rows = rows < 0 ? 0 : (rows > CR ? CR : rows);
+        int flags = khf & kSegComplete;
+        if (j == 0) flags |= khf & kSegStart;
+        if (j == nck - 1) flags |= khf & kSegEnd;
+        ck->flags = flags;
+        if (++j == nck) {
+            j = 0;
+            ++cur;
+        }
+        return true;
+    }
+};
+
+}  // namespace pd

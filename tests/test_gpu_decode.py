@@ -60,8 +60,10 @@ def test_dtype_headdim_group_grid(dtype, head_dim, hq, hk):
 
 
 @pytest.mark.parametrize("page_size", [1, 8, 16, 32, 64, 100])
-def test_page_sizes(page_size):
-    w = wl.make_paged(f"pages_{page_size}", "bf16", [1, page_size, 2 * page_size, 333, 50], 16, 4, 128,
+@pytest.mark.parametrize("hq,hk,dtype", [(16, 4, "bf16"), (16, 2, "bf16"), (16, 2, "f16")])
+def test_page_sizes(page_size, hq, hk, dtype):
+    # group 4 runs on CUDA cores, group 8 on the tensor-core kernel (16-row TMA boxes)
+    w = wl.make_paged(f"pages_{page_size}", dtype, [1, page_size, 2 * page_size, 333, 50, 17], hq, hk, 128,
                       page_size, seed=40 + page_size)
     _run(w)
 
