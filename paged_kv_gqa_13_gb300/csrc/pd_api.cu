@@ -10,7 +10,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "../../include/pagedecode.h"
+#include "pagedecode.h"
 #include "pd_kernels.cuh"
 
 namespace pd {

@@ -75,7 +75,6 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const bool staged = a.table_bytes > 0;
     int* s_indptr = reinterpret_cast<int*>(smem);
     int* s_lpl = s_indptr + kTableMax + 1;
     uint8_t* wsm = smem + a.table_bytes + wid * C::kWarpBytes;
@@ -93,19 +92,18 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     const int GT = a.heads_per_tile;
 
     // ---- set-up: stage the page table, zero the ring, init the barriers
-    if (staged) {
-        for (int x = threadIdx.x; x <= a.batch; x += blockDim.x) s_indptr[x] = __ldg(a.indptr + x);
-        for (int x = threadIdx.x; x < a.batch; x += blockDim.x) s_lpl[x] = __ldg(a.last_page_len + x);
-    }
-    // Rows of a stage that no copy fills must still hold finite numbers, since
-    // their (zero) softmax weight multiplies them.
-    for (int off = lane * 16; off < kStages * C::kStageBytes; off += 32 * 16)
-        *reinterpret_cast<uint4*>(wsm + off) = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_mbar_init();
-    }
+    walk.stage_table(s_indptr, s_lpl, [&] {
+        // Rows of a stage that no copy fills must still hold finite numbers,
+        // since their (zero) softmax weight multiplies them.
+        for (int off = lane * 16; off < kStages * C::kStageBytes; off += 32 * 16)
+            *reinterpret_cast<uint4*>(wsm + off) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+            fence_mbar_init();
+        }
+        walk.prefetch_first_slabs(first_page, kStages, size_t(C::kRowBytes));
+    });
     __syncthreads();  // the only block-wide barrier: warps are independent from here on
     // Let the merge kernel be scheduled now; it waits for this grid before it
     // reads any partial result.
@@ -187,68 +185,50 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     };
     reset_state();
 
+    // End of this warp's share of a request: sum the row groups' accumulators
+    // (a reduce-scatter, so each lane ends up owning a share of the columns
+    // of the group's heads), then write o and lse, or the normalised partial.
+    using RSR = ReduceScatter2<G * kEp2, 16, kL>;
+    constexpr int kOwn = (kRW > 1) ? G * kEp2 / kRW : G * kEp2;  // float2 values a lane writes
     auto finalize = [&](int4 m) {
-        float lh[G];
+        float lh[G], inv[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < kVF; ++j) s += (primary && hj[j] == h) ? lmy[j] : 0.f;
             lh[h] = warp_sum(s);
+            inv[h] = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
         }
-#pragma unroll
-        for (int off = kL; off < 32; off <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < kEp2; ++e) {
-                    acc[h][e].x += __shfl_xor_sync(kFull, acc[h][e].x, off);
-                    acc[h][e].y += __shfl_xor_sync(kFull, acc[h][e].y, off);
-                }
+        float2* flat = &acc[0][0];
+        RSR::run(flat, lane);
         const int qrow = m.z;  // first q / o row of the group
-        if (m.y & kSegComplete) {
-            if (lane < kL) {
+        const bool complete = (m.y & kSegComplete) != 0;
+        const long long slot = gwarp + m.w;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    if (h >= GT) break;
-                    const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
-                    T* orow = static_cast<T*>(a.o) + (size_t(qrow) + h) * D;
-#pragma unroll
-                    for (int nv = 0; nv < kNvec; ++nv) {
-                        float f[kVec];
-#pragma unroll
-                        for (int e = 0; e < kVec / 2; ++e) {
-                            f[2 * e] = acc[h][nv * kVec / 2 + e].x * inv;
-                            f[2 * e + 1] = acc[h][nv * kVec / 2 + e].y * inv;
-                        }
-                        *reinterpret_cast<uint4*>(orow + (nv * kL + c) * kVec) = E::from_f32(f);
-                    }
+        for (int j = 0; j < kOwn; ++j) {
+            const int x = RSR::index(j, lane);
+            const int h = x / kEp2, e = 2 * (x % kEp2);
+            if (h >= GT) continue;
+            const int d = ((e / kVec) * kL + c) * kVec + (e % kVec);
+            const float iv = pick(inv, h);
+            const float2 val = make_float2(flat[j].x * iv, flat[j].y * iv);
+            if (complete) {
+                T* orow = static_cast<T*>(a.o) + (size_t(qrow) + h) * D;
+                if constexpr (sizeof(T) == 4) {
+                    *reinterpret_cast<float2*>(orow + d) = val;
+                } else {
+                    *reinterpret_cast<uint32_t*>(orow + d) = E::pack(val.x, val.y);
                 }
+            } else {
+                *reinterpret_cast<float2*>(a.part_o + (size_t(slot) * G + h) * D + d) = val;
             }
-            if (a.lse != nullptr && lane < GT) {
-                const float l = pick(lh, lane), mr = pick(mref, lane);
-                a.lse[size_t(qrow) + lane] = l > 0.f ? (mr + log2f(l)) * kLn2 : kNegInf;
-            }
-        } else {
-            const long long slot = gwarp + m.w;
-            if (lane < kL) {
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    if (h >= GT) break;
-                    const float inv = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
-                    float* prow = a.part_o + (size_t(slot) * G + h) * D;
-#pragma unroll
-                    for (int nv = 0; nv < kNvec; ++nv)
-#pragma unroll
-                        for (int e4 = 0; e4 < kVec / 2; e4 += 2) {
-                            const float2 u = acc[h][nv * kVec / 2 + e4], w2 = acc[h][nv * kVec / 2 + e4 + 1];
-                            *reinterpret_cast<float4*>(prow + (nv * kL + c) * kVec + 2 * e4) =
-                                make_float4(u.x * inv, u.y * inv, w2.x * inv, w2.y * inv);
-                        }
-                }
-            }
-            if (lane < GT) {
-                const float l = pick(lh, lane), mr = pick(mref, lane);
+        }
+        if (lane < GT) {
+            const float l = pick(lh, lane), mr = pick(mref, lane);
+            if (complete) {
+                if (a.lse != nullptr) a.lse[size_t(qrow) + lane] = l > 0.f ? (mr + log2f(l)) * kLn2 : kNegInf;
+            } else {
                 a.part_lse[size_t(slot) * G + lane] = l > 0.f ? mr + log2f(l) : kNegInf;
             }
         }

@@ -80,7 +80,6 @@ __global__ void __launch_bounds__(256, 1)
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const bool staged = a.table_bytes > 0;
     int* s_indptr = reinterpret_cast<int*>(smem);
     int* s_lpl = s_indptr + kTableMax + 1;
     uint8_t* wsm = smem + a.table_bytes + wid * C::kWarpBytes;
@@ -99,14 +98,13 @@ __global__ void __launch_bounds__(256, 1)
         prefetch_tensormap(&tmv);
     }
 
-    if (staged) {
-        for (int x = threadIdx.x; x <= a.batch; x += blockDim.x) s_indptr[x] = __ldg(a.indptr + x);
-        for (int x = threadIdx.x; x < a.batch; x += blockDim.x) s_lpl[x] = __ldg(a.last_page_len + x);
-    }
-    if (lane == 0) {
-        for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_mbar_init();
-    }
+    walk.stage_table(s_indptr, s_lpl, [&] {
+        if (lane == 0) {
+            for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
+            fence_mbar_init();
+        }
+        walk.prefetch_first_slabs(first_page, kS, size_t(D) * sizeof(T));
+    });
     __syncthreads();  // the only block-wide barrier
     launch_dependents();
     if (p0 >= pend) return;

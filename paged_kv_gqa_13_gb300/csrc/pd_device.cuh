@@ -105,6 +105,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (no shared memory, no
+// completion). src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 4-D tiled tensor copy global -> shared through a tensor map (TMA), with
 // completion counted in bytes on `bar`. The innermost coordinate c0 is in
 // elements; c0 * element size must be a multiple of 16 bytes.
@@ -285,6 +291,37 @@ struct ReduceScatter {
             return j;
         } else {
             return ReduceScatter<N / 2, OFF / 2>::index(j, lane) + (((lane & OFF) != 0) ? N / 2 : 0);
+        }
+    }
+};
+
+// Reduce-scatter of N float2 values across the lanes that differ in the bits
+// OFF, OFF/2, ..., STOP (lane bits of the row groups): after it a lane holds
+// N / (OFF*2/STOP) complete sums, those of the indices given by index().
+template <int N, int OFF, int STOP>
+struct ReduceScatter2 {
+    __device__ static __forceinline__ void run(float2* v, int lane) {
+        if constexpr (OFF < STOP || OFF == 0) {
+            return;
+        } else {
+            static_assert(N >= 2, "one value per lane is the finest split");
+            constexpr int H = N / 2;
+            const bool up = (lane & OFF) != 0;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const float2 send = up ? v[j] : v[j + H];
+                const float2 keep = up ? v[j + H] : v[j];
+                const float2 got = make_float2(__shfl_xor_sync(kFull, send.x, OFF), __shfl_xor_sync(kFull, send.y, OFF));
+                v[j] = __fadd2_rn(keep, got);
+            }
+            ReduceScatter2<H, OFF / 2, STOP>::run(v, lane);
+        }
+    }
+    __device__ static __forceinline__ int index(int j, int lane) {
+        if constexpr (OFF < STOP || OFF == 0) {
+            return j;
+        } else {
+            return ReduceScatter2<N / 2, OFF / 2, STOP>::index(j, lane) + (((lane & OFF) != 0) ? N / 2 : 0);
         }
     }
 };

@@ -13,6 +13,39 @@ template <int kPer, class LseAt, class RowAt>
 __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_at, float* acc) {
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;
+    constexpr int kFast = (64 / kPer) < 16 ? (64 / kPer) : 16;  // parts kept in registers
+    if (parts <= kFast) {
+        // One round trip: every part's lse and row are requested before any
+        // weight is known.
+        float rows[kFast][kPer];
+#pragma unroll
+        for (int cp = 0; cp < kFast; ++cp) {
+            if (cp < parts) {
+                const float* po = row_at(cp) + lane * kPer;
+#pragma unroll
+                for (int e = 0; e < kPer; e += 2) {
+                    const float2 t = *reinterpret_cast<const float2*>(po + e);
+                    rows[cp][e] = t.x;
+                    rows[cp][e + 1] = t.y;
+                }
+            }
+        }
+        const float mine = lane < parts ? lse_at(lane) : kNegInf;
+        const float M = warp_max(mine);
+        if (M == kNegInf) return kNegInf;
+        const float S = warp_sum(lane < parts ? ex2(mine - M) : 0.f);
+        const float L = M + log2f(S);
+        const float w_mine = lane < parts ? ex2(mine - L) : 0.f;
+#pragma unroll
+        for (int cp = 0; cp < kFast; ++cp) {
+            const float w = __shfl_sync(kFull, w_mine, cp);
+            if (cp < parts) {
+#pragma unroll
+                for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, rows[cp][e], acc[e]);
+            }
+        }
+        return L;
+    }
     float M = kNegInf;
     for (int cp = lane; cp < parts; cp += 32) M = fmaxf(M, lse_at(cp));
     M = warp_max(M);
@@ -24,15 +57,27 @@ __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_a
     for (int base = 0; base < parts; base += 32) {
         const int n = min(32, parts - base);
         const float w_mine = (lane < n) ? ex2(lse_at(base + lane) - L) : 0.f;
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-            const float w = __shfl_sync(kFull, w_mine, j);
-            const float* po = row_at(base + j) + lane * kPer;
+        for (int j0 = 0; j0 < n; j0 += 8) {
+            float rows[8][kPer];  // eight rows in flight before any is used
 #pragma unroll
-            for (int e = 0; e < kPer; e += 2) {
-                const float2 t = *reinterpret_cast<const float2*>(po + e);
-                acc[e] = fmaf(w, t.x, acc[e]);
-                acc[e + 1] = fmaf(w, t.y, acc[e + 1]);
+            for (int j = 0; j < 8; ++j) {
+                if (j0 + j < n) {
+                    const float* po = row_at(base + j0 + j) + lane * kPer;
+#pragma unroll
+                    for (int e = 0; e < kPer; e += 2) {
+                        const float2 t = *reinterpret_cast<const float2*>(po + e);
+                        rows[j][e] = t.x;
+                        rows[j][e + 1] = t.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
+                if (j0 + j < n) {
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, rows[j][e], acc[e]);
+                }
             }
         }
     }
@@ -59,7 +104,7 @@ __device__ __forceinline__ void store_row(T* orow, const float* acc) {
 // not depend on the decode's output (the page table, empty requests) is done
 // before waiting for the decode grid.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_partials_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(128, 1) merge_partials_kernel(const MergeArgs a) {
     constexpr int kPer = D / 32;  // elements per lane
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;

@@ -145,6 +145,61 @@ struct Walk {
         return load_page(p0 + lane);
     }
 
+    // Start pulling the K/V slabs of this warp's first `count` positions into
+    // L2 as soon as their page ids are known, before the page table needed to
+    // describe them has been staged. Whole slabs: pages hold page_size rows;
+    // contiguous slabs are clipped to the cache.
+    __device__ __forceinline__ void prefetch_first_slabs(int pg, int count, size_t row_bytes) {
+        const long long p = p0 + lane;
+        if (lane >= count || p >= pend) return;
+        const int sh = int(p / a.n_pos), i = int(p % a.n_pos);
+        const int kh = sh / a.head_tiles;
+        size_t row;
+        long long rows;
+        if (contiguous) {
+            const int b = i / a.npv;
+            const long long r0 = (long long)(i % a.npv) * a.vpage;
+            rows = min((long long)a.vpage, a.slab_rows - r0);
+            row = (size_t(b) * a.num_kv_heads + kh) * size_t(a.slab_rows) + size_t(r0);
+        } else {
+            if (pg < 0 || pg >= a.num_total_pages) return;
+            rows = a.page_size;
+            row = (size_t(pg) * a.num_kv_heads + kh) * size_t(a.slab_rows);
+        }
+        if (rows <= 0) return;
+        const uint32_t bytes = uint32_t(rows * (long long)row_bytes);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.k) + row * row_bytes, bytes);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.v) + row * row_bytes, bytes);
+    }
+
+    // Copy indptr and last_page_len into shared memory. The loads are issued
+    // first and stored after `overlap()` runs, so that their latency hides it.
+    template <class F>
+    __device__ __forceinline__ void stage_table(int* si, int* sl, F overlap) {
+        constexpr int kPer = (kTableMax + 1 + 255) / 256;  // entries per thread at 256 threads
+        int vi[kPer], vl[kPer];
+        const int nt = blockDim.x;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int x = threadIdx.x + k * nt;
+            vi[k] = (staged && x <= a.batch) ? __ldg(a.indptr + x) : 0;
+            vl[k] = (staged && x < a.batch) ? __ldg(a.last_page_len + x) : 0;
+        }
+        overlap();
+        if (!staged) return;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int x = threadIdx.x + k * nt;
+            if (x <= a.batch) si[x] = vi[k];
+            if (x < a.batch) sl[x] = vl[k];
+        }
+        // entries past kPer * blockDim (only with fewer than 256 threads)
+        for (int x = threadIdx.x + kPer * nt; x <= a.batch; x += nt) {
+            si[x] = __ldg(a.indptr + x);
+            if (x < a.batch) sl[x] = __ldg(a.last_page_len + x);
+        }
+    }
+
     // The next chunk of at most CR rows; false when the range is exhausted.
     template <int CR>
     __device__ __forceinline__ bool next(Chunk* ck) {
