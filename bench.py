@@ -36,7 +36,8 @@ METRIC = "achieved HBM TB/s (% of GB300 peak) and us per batched paged-decode ca
 UNIT = "TB/s"
 DEFAULT_CONFIG = "llama3_8b"
 L2_FLUSH_BYTES = 512 << 20
-KERNEL_SOURCES = ["paged_kv_gqa_13_gb300/csrc/pd_decode.cuh", "paged_kv_gqa_13_gb300/csrc/pd_device.cuh"]
+KERNEL_SOURCES = ["paged_kv_gqa_13_gb300/csrc/" + f for f in
+                  ("pd_device.cuh", "pd_walk.cuh", "pd_decode.cuh", "pd_decode_mma.cuh", "pd_merge.cuh")]
 
 
 def kernel_sha() -> str:
@@ -137,6 +138,15 @@ def load_workload(name: str, rank: int = 0):
     if name == "long_context_contiguous":
         return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous"
     return wl.CONFIGS[name](seed=wl.CONFIGS[name].__defaults__[0] + 100 * rank), "paged"
+
+
+def decode_kernel_name(w) -> str:
+    """The decode kernel the library picks for this workload (tensor cores for
+    16-bit tiles of 5..8 q heads per kv head, CUDA cores otherwise)."""
+    g = w.group
+    tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
+    per_tile = g // tiles
+    return "decode_mma_kernel" if (w.dtype != "f32" and per_tile > 4) else "decode_kernel"
 
 
 def algorithmic_bytes(w, table=None) -> int:
@@ -406,10 +416,11 @@ def main():
     dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
     dec_bytes = r["bytes_mean"]
     achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
-    traffic = recorded_traffic("decode_kernel", w.name)
+    kname = decode_kernel_name(w)
+    traffic = recorded_traffic(kname, w.name + ("/contiguous" if r["mode"] == "contiguous" else ""))
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
-                "peak_source": peaks["source"], "kernel": "decode_kernel",
+                "peak_source": peaks["source"], "kernel": kname,
                 "kernel_us": dec_ms * 1e3, "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
                 "copy_kernel_gbs": r["copy_gbs"],
                 "timing": "kernel events from a second pass over the same K steps"}
