@@ -296,38 +296,75 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     # page table in from pinned host memory, decode, copy o and lse out.
     e2e = None
     if mode == "paged" and not w.append_steps and not args.quick:
+        # One step end to end: the step's inputs (q and the page table) go in
+        # from pinned host memory in one copy, the decode runs, o and lse come
+        # back in one copy. The KV cache is resident state, like weights.
         t = tables[0]
-        hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16 if w.dtype != "f32" else np.float32)).pin_memory()
-        h_ind = torch.from_numpy(t.indices.astype(np.int32)).pin_memory()
-        h_ptr = torch.from_numpy(t.indptr.astype(np.int32)).pin_memory()
-        h_lpl = torch.from_numpy(t.last_page_len.astype(np.int32)).pin_memory()
-        h_o = torch.empty(o.numel() * o.element_size(), dtype=torch.uint8).pin_memory()
-        h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        d_ind, d_ptr, d_lpl = dev_tables[0]
-        q_raw = q.view(torch.int16) if w.dtype != "f32" else q
-        h2d = hq.numel() * hq.element_size() + 4 * (h_ind.numel() + h_ptr.numel() + h_lpl.numel())
-        d2h = h_o.numel() + 4 * h_lse.numel()
+        esz = q.element_size()
+        parts_in = [("q", q.numel() * esz), ("indices", 4 * t.num_indices), ("indptr", 4 * (w.batch + 1)),
+                    ("lpl", 4 * w.batch)]
+        offs, n = {}, 0
+        for name, nb in parts_in:
+            offs[name] = n
+            n += (nb + 15) // 16 * 16  # keep every view 16-byte aligned
+        h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d_in = torch.empty(n, dtype=torch.uint8, device=dev)
+        q_host = np.ascontiguousarray(w.q).view(np.uint8).reshape(-1)
+        h_in[offs["q"]:offs["q"] + q_host.size] = torch.from_numpy(q_host)
+        for name, arr in (("indices", t.indices), ("indptr", t.indptr), ("lpl", t.last_page_len)):
+            b = np.ascontiguousarray(arr.astype(np.int32)).view(np.uint8).reshape(-1)
+            h_in[offs[name]:offs[name] + b.size] = torch.from_numpy(b)
+
+        def view(buf, name, nbytes, dtype, shape):
+            return buf[offs[name]:offs[name] + nbytes].view(dtype).view(shape)
+        qd = view(d_in, "q", q.numel() * esz, q.dtype, q.shape)
+        ind_d = view(d_in, "indices", 4 * t.num_indices, torch.int32, (t.num_indices,))
+        ptr_d = view(d_in, "indptr", 4 * (w.batch + 1), torch.int32, (w.batch + 1,))
+        lpl_d = view(d_in, "lpl", 4 * w.batch, torch.int32, (w.batch,))
+        ob = o.numel() * esz
+        d_out = torch.empty(ob + 4 * lse.numel(), dtype=torch.uint8, device=dev)
+        h_out = torch.empty_like(d_out, device="cpu").pin_memory()
+        od = d_out[:ob].view(q.dtype).view(o.shape)
+        lsed = d_out[ob:].view(torch.float32).view(lse.shape)
         es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        host_s = []
         for i in range(args.warmup + args.steps):
             if i >= args.warmup:
                 flush_l2()
                 es[2 * (i - args.warmup)].record(stream)
-            q_raw.copy_(hq, non_blocking=True)
-            d_ind.copy_(h_ind, non_blocking=True)
-            d_ptr.copy_(h_ptr, non_blocking=True)
-            d_lpl.copy_(h_lpl, non_blocking=True)
-            pd.pd_paged_decode(q, k, v, d_ind, d_ptr, d_lpl, o, lse, w.sm_scale, ws)
-            h_o.copy_(o.view(torch.uint8).view(-1), non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
+            h0 = time.perf_counter()
+            d_in.copy_(h_in, non_blocking=True)
+            pd.pd_paged_decode(qd, k, v, ind_d, ptr_d, lpl_d, od, lsed, w.sm_scale, ws)
+            h_out.copy_(d_out, non_blocking=True)
+            host_s.append(time.perf_counter() - h0)
             if i >= args.warmup:
                 es[2 * (i - args.warmup) + 1].record(stream)
         torch.cuda.synchronize()
         e2e_ms = float(np.mean([es[2 * j].elapsed_time(es[2 * j + 1]) for j in range(args.steps)]))
         e2e = {"value": bytes_mean / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(n), "d2h_bytes_per_step": int(d_out.numel()),
+               "host_us_per_step": 1e6 * float(np.median(host_s[args.warmup:]))}
     clocks = sampler.stop()
     return {"w": w, "mode": mode, "ms_mean": ms_mean, "ms_all": ms, "bytes_mean": bytes_mean, "prof": prof,
             "copy_gbs": copy_gbs, "e2e": e2e, "clocks": clocks, "t_wall": t_wall}
+
+
+def slowest_rank_ms(ms_local: float, world: int) -> float:
+    """Step time of the whole job: the maximum of the ranks' mean step times."""
+    if world == 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tbps(bytes_per_rank: float, ms_max: float, world: int) -> float:
+    """Every rank decodes its own batch (replicas, weak scaling): total bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def cpu_baseline(w, mode: str, budget_s: float = 12.0) -> dict:
@@ -397,20 +434,13 @@ def main():
 
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     r = run_gpu(args, rank, world, local_rank)
-    ms_max = r["ms_mean"]
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-
-        t = torch.tensor([ms_max], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = slowest_rank_ms(r["ms_mean"], world)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
     w = r["w"]
-    tbps = world * r["bytes_mean"] / (ms_max * 1e-3) / 1e12
+    tbps = whole_job_tbps(r["bytes_mean"], ms_max, world)
     peaks = measured_peaks()
     prof = r["prof"]
     dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])

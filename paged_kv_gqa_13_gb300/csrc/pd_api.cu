@@ -121,7 +121,43 @@ void split_group(int g, int* tiles, int* per) {
     *per = g / t;
 }
 
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p);
+
+// Plans depend only on the shape and the device: keep the last few so that a
+// decode loop pays the occupancy query and the attribute set-up once.
 pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p) {
+    struct Entry {
+        int dev;
+        pd_dtype dt;
+        int batch, Hq, Hk, D;
+        bool contiguous;
+        Plan plan;
+    };
+    static Entry cache[16];
+    static int used = 0, next = 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = cache[i];
+            if (e.dev == dev && e.dt == dt && e.batch == batch && e.Hq == Hq && e.Hk == Hk && e.D == D &&
+                e.contiguous == contiguous) {
+                *p = e.plan;
+                return PD_OK;
+            }
+        }
+    }
+    const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, p);
+    if (st != PD_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, *p};
+    next = (next + 1) % 16;
+    if (used < 16) ++used;
+    return PD_OK;
+}
+
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p) {
     if (dt != PD_F32 && dt != PD_F16 && dt != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || Hq <= 0 || Hk <= 0) return fail(PD_ERR_INVALID, "batch, num_qo_heads and num_kv_heads must be positive");
     if (Hq % Hk != 0) return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", Hq, Hk);
