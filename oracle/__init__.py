@@ -22,6 +22,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
 _SO = os.path.join(_HERE, "liboracle.so")
+# A test that plants a mistake in the oracle points this at a mutant build.
+_OVERRIDE = os.environ.get("PD_ORACLE_LIBRARY")
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 
@@ -45,7 +47,7 @@ _L = ctypes.c_long
 def _lib():
     global _handle
     if _handle is None:
-        lib = ctypes.CDLL(build())
+        lib = ctypes.CDLL(_OVERRIDE or build())
         lib.oracle_decode_elements.argtypes = [_P, _I, _L, _P]
         lib.oracle_paged_decode.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _L,
                                             ctypes.c_float, _I, _P, _P, _I]

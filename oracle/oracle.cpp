@@ -18,6 +18,13 @@
 //  [P2] ferrox-cuda 0.15.2, src/attn.rs: gqa_decode (the q-head to kv-head
 //       map kv_h = h / (n_heads / n_kv_heads); zero output for an empty cache).
 //
+// ORACLE_MUTANT (compile-time, never set in a normal build) plants one known
+// mistake; tests/test_oracle_mutants.py builds each mutant and checks that the
+// pins in tests/test_oracle.py fail on it.
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+//
 // Readings where the pages are silent (each also listed in the design notes):
 //  - lse is the natural log of the sum of exp(scaled score): lse = m + ln(Z).
 //  - sm_scale multiplies q.k before the softmax, so lse is over scaled scores.
@@ -117,7 +124,7 @@ void attend(const View& q, size_t q_off, long n, int D, double scale, KAt k_at, 
     for (long t = 0; t < n; ++t) {
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += q.at(q_off + d) * k_at(t, d);
-        s[size_t(t)] = scale * dot;
+        s[size_t(t)] = (ORACLE_MUTANT == 1 ? 1.0 : scale) * dot;  // mutant 1: scale dropped
     }
     double m = s[0];
     for (long t = 1; t < n; ++t) m = s[size_t(t)] > m ? s[size_t(t)] : m;
@@ -126,10 +133,10 @@ void attend(const View& q, size_t q_off, long n, int D, double scale, KAt k_at, 
     for (long t = 0; t < n; ++t) {
         const double w = std::exp(s[size_t(t)] - m);
         Z += w;
-        for (int d = 0; d < D; ++d) acc[size_t(d)] += w * v_at(t, d);
+        for (int d = 0; d < D; ++d) acc[size_t(d)] += w * (ORACLE_MUTANT == 2 ? k_at(t, d) : v_at(t, d));
     }
-    for (int d = 0; d < D; ++d) o[d] = acc[size_t(d)] / Z;
-    *lse = m + std::log(Z);
+    for (int d = 0; d < D; ++d) o[d] = ORACLE_MUTANT == 3 ? acc[size_t(d)] : acc[size_t(d)] / Z;
+    *lse = ORACLE_MUTANT == 4 ? m + std::log2(Z) : m + std::log(Z);
 }
 
 }  // namespace
@@ -174,12 +181,12 @@ int oracle_paged_decode(const void* q, const void* k_data, const void* v_data,
     const double scale = double(sm_scale);
     parallel_for(long(batch) * num_qo_heads, nthreads, [&](long bh) {
         const int b = int(bh / num_qo_heads), h = int(bh % num_qo_heads);
-        const int kh = h / group;  // [P2] gqa_decode: kv_h = h / group_size
+        const int kh = ORACLE_MUTANT == 5 ? h % num_kv_heads : h / group;  // [P2] gqa_decode: kv_h = h / group_size
         const long np = indptr[b + 1] - indptr[b];
-        const long n = np == 0 ? 0 : (np - 1) * page_size + last_page_len[b];
+        const long n = np == 0 ? 0 : (np - 1) * page_size + (ORACLE_MUTANT == 6 ? page_size : last_page_len[b]);
         auto addr = [&](long t, int d) {
             const size_t page = size_t(indices[indptr[b] + t / page_size]);
-            const size_t row = size_t(t % page_size);
+            const size_t row = size_t(ORACLE_MUTANT == 7 ? page_size - 1 - t % page_size : t % page_size);
             return ((page * num_kv_heads + kh) * page_size + row) * head_dim + size_t(d);
         };
         attend(Q, size_t(bh) * head_dim, n, head_dim, scale,
@@ -232,7 +239,7 @@ int oracle_paged_append(const void* k_new, const void* v_new, void* k_data, void
     const size_t eb = elem_bytes(dtype), row = size_t(head_dim) * eb;
     for (int b = 0; b < batch; ++b) {
         if (indptr[b + 1] <= indptr[b]) return 2;
-        const int slot = last_page_len[b] - 1;
+        const int slot = ORACLE_MUTANT == 8 ? last_page_len[b] % page_size : last_page_len[b] - 1;
         const int page = indices[indptr[b + 1] - 1];
         if (slot < 0 || slot >= page_size || page < 0 || page >= num_total_pages) return 2;
         for (int h = 0; h < num_kv_heads; ++h) {
@@ -268,7 +275,7 @@ int oracle_merge_states(const double* o_parts, const double* lse_parts, int num_
         const double L = M + std::log(S);
         for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
         for (int c = 0; c < num_parts; ++c) {
-            const double w = std::exp(lse_parts[size_t(c) * rows + r] - L);
+            const double w = std::exp(ORACLE_MUTANT == 9 ? L - lse_parts[size_t(c) * rows + r] : lse_parts[size_t(c) * rows + r] - L);
             const double* oc = o_parts + (size_t(c) * rows + r) * head_dim;
             for (int d = 0; d < head_dim; ++d) o[d] += w * oc[d];
         }
