@@ -55,9 +55,11 @@ def _lib():
                                                  _I, _P, _P, _I]
         lib.oracle_paged_append.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]
         lib.oracle_merge_states.argtypes = [_P, _P, _I, _L, _I, _P, _P]
+        lib.oracle_contiguous_append.argtypes = [_P, _P, _P, _P, _I, _I, _I, _L, _L, _I]
         lib.oracle_round_to_dtype.argtypes = [_P, _L, _I, _P]
         for f in (lib.oracle_decode_elements, lib.oracle_paged_decode, lib.oracle_contiguous_decode,
-                  lib.oracle_paged_append, lib.oracle_merge_states, lib.oracle_round_to_dtype):
+                  lib.oracle_paged_append, lib.oracle_merge_states, lib.oracle_round_to_dtype,
+                  lib.oracle_contiguous_append):
             f.restype = _I
         lib.oracle_hardware_threads.restype = _I
         _handle = lib
@@ -145,6 +147,18 @@ def paged_append(k_new, v_new, k_data, v_data, indices, indptr, last_page_len, d
                                     head_dim, page_size, num_total_pages, DTYPE_CODE[dtype])
     if rc:
         raise OracleError(f"oracle_paged_append returned {rc}")
+
+
+def contiguous_append(k_new, v_new, k_cache, v_cache, position, dtype):
+    """Write row `position` of every (request, kv head) of the host mirrors in place."""
+    k_new, v_new = _c(k_new), _c(v_new)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    batch, num_kv_heads, max_kv_len, head_dim = k_cache.shape
+    rc = _lib().oracle_contiguous_append(k_new.ctypes.data, v_new.ctypes.data, k_cache.ctypes.data,
+                                         v_cache.ctypes.data, batch, num_kv_heads, head_dim, max_kv_len,
+                                         int(position), DTYPE_CODE[dtype])
+    if rc:
+        raise OracleError(f"oracle_contiguous_append returned {rc}")
 
 
 def merge_states(o_parts, lse_parts):

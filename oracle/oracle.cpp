@@ -252,6 +252,27 @@ int oracle_paged_append(const void* k_new, const void* v_new, void* k_data, void
     return 0;
 }
 
+// Append to a contiguous cache ([P3] "Companion plans": KvCacheAppendPlan, the
+// rank-4 cache with no page table): for every request b and kv head h, row
+// `position` of k_cache[b, h, :, :] becomes k_new[b, h, :], the same for v.
+// k_cache/v_cache [batch, num_kv_heads, max_kv_len, head_dim]. Returns 0 or 1.
+int oracle_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
+                             int num_kv_heads, int head_dim, long max_kv_len, long position, int dtype) {
+    if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len <= 0 || position < 0 ||
+        position >= max_kv_len || dtype < 0 || dtype > 2)
+        return 1;
+    const size_t row = size_t(head_dim) * elem_bytes(dtype);
+    for (int b = 0; b < batch; ++b)
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const long pos = ORACLE_MUTANT == 10 ? (position > 0 ? position - 1 : position + 1) : position;
+            const size_t dst = ((size_t(b) * num_kv_heads + h) * size_t(max_kv_len) + size_t(pos)) * row;
+            const size_t src = (size_t(b) * num_kv_heads + h) * row;
+            std::memcpy(static_cast<uint8_t*>(k_cache) + dst, static_cast<const uint8_t*>(k_new) + src, row);
+            std::memcpy(static_cast<uint8_t*>(v_cache) + dst, static_cast<const uint8_t*>(v_new) + src, row);
+        }
+    return 0;
+}
+
 // Merge of attention states computed over disjoint key sets into the state over
 // their union: L = ln sum_c exp(lse_c), o = sum_c exp(lse_c - L) * o_c. With
 // M = max_c lse_c, L = M + ln sum_c exp(lse_c - M). All parts empty (every

@@ -363,3 +363,25 @@ def test_append_writes_the_new_last_token():
                                      w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale, "f16")
         vnv = oracle.decode_elements(vn, "f16")
         np.testing.assert_allclose(o, vnv, rtol=0, atol=1e-6)
+
+
+def test_contiguous_append_writes_the_new_last_row():
+    # After appending at position n, a contiguous decode over n + 1 rows with a
+    # query aligned to the new key returns the new value row, and only the new
+    # rows of the cache changed. Catches: writing row n - 1 or row n + 1.
+    B, Hk, L, D, n = 3, 4, 40, 64, 25
+    kc = wl.normal((B, Hk, L, D), "f16", wl.stream_key(140, "k"))
+    vc = wl.normal((B, Hk, L, D), "f16", wl.stream_key(140, "v"))
+    kn = wl.normal((B, Hk, D), "f16", wl.stream_key(140, "k_new"))
+    vn = wl.normal((B, Hk, D), "f16", wl.stream_key(140, "v_new"))
+    before = kc.copy()
+    oracle.contiguous_append(kn, vn, kc, vc, n, "f16")
+    changed = np.argwhere(np.any(kc != before, axis=-1))
+    assert {tuple(x[2:]) for x in changed} == {(n,)}
+    knv = oracle.decode_elements(kn, "f16")
+    qf = knv * (60.0 / np.maximum((knv * knv).sum(-1, keepdims=True) * 0.125, 1e-3))
+    q = wl.round_f32(qf.astype(np.float32), "f16")
+    o, _ = oracle.contiguous_decode(q, kc, vc, Hk, n + 1, 0.125, "f16")
+    np.testing.assert_allclose(o, oracle.decode_elements(vn, "f16"), rtol=0, atol=1e-6)
+    with pytest.raises(oracle.OracleError):
+        oracle.contiguous_append(kn, vn, kc, vc, L, "f16")

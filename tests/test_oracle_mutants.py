@@ -20,6 +20,7 @@ MUTANTS = {
     7: "rows of a page read in reverse",
     8: "append writes slot last_page_len instead of last_page_len - 1",
     9: "merge weights exp(L - lse_c) instead of exp(lse_c - L)",
+    10: "contiguous append one row early",
 }
 
 
