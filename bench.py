@@ -193,6 +193,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         def step(i):
             pd.pd_contiguous_decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
         bytes_per_step = [algorithmic_bytes(w)]
+        decode_bytes_per_step = bytes_per_step
     else:
         k = to_dev(w.k_data, w.dtype, dev)
         v = to_dev(w.v_data, w.dtype, dev)
@@ -222,6 +223,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                 ind, ptr, lpl = dev_tables[0]
             pd.pd_paged_decode(q, k, v, ind, ptr, lpl, o, lse, w.sm_scale, ws)
         bytes_per_step = [algorithmic_bytes(w, t) for t in tables]
+        decode_bytes_per_step = list(bytes_per_step)
         if w.append_steps:
             ab = 2 * w.batch * w.num_kv_heads * w.head_dim * wl.ELEM_BYTES[w.dtype] * 2
             bytes_per_step = [b + ab for b in bytes_per_step]
@@ -291,6 +293,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     ms_mean = float(np.mean(ms))
     byte_steps = [bytes_per_step[(args.warmup + i) % len(bytes_per_step)] for i in range(args.steps)]
     bytes_mean = float(np.mean(byte_steps))
+    decode_bytes_mean = float(np.mean([decode_bytes_per_step[(args.warmup + i) % len(decode_bytes_per_step)]
+                                       for i in range(args.steps)]))
 
     # end to end through the C ABI with host buffers: per step, copy q and the
     # page table in from pinned host memory, decode, copy o and lse out.
@@ -345,7 +349,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                "h2d_bytes_per_step": int(n), "d2h_bytes_per_step": int(d_out.numel()),
                "host_us_per_step": 1e6 * float(np.median(host_s[args.warmup:]))}
     clocks = sampler.stop()
-    return {"w": w, "mode": mode, "ms_mean": ms_mean, "ms_all": ms, "bytes_mean": bytes_mean, "prof": prof,
+    return {"w": w, "mode": mode, "ms_mean": ms_mean, "ms_all": ms, "bytes_mean": bytes_mean,
+            "decode_bytes_mean": decode_bytes_mean, "prof": prof,
             "copy_gbs": copy_gbs, "e2e": e2e, "clocks": clocks, "t_wall": t_wall}
 
 
@@ -444,7 +449,7 @@ def main():
     peaks = measured_peaks()
     prof = r["prof"]
     dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
-    dec_bytes = r["bytes_mean"]
+    dec_bytes = r["decode_bytes_mean"]  # the decode kernel's own bytes (no append rows)
     achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
     kname = decode_kernel_name(w)
     traffic = recorded_traffic(kname, w.name + ("/contiguous" if r["mode"] == "contiguous" else ""))
@@ -452,11 +457,12 @@ def main():
                 "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
                 "peak_source": peaks["source"], "kernel": kname,
                 "kernel_us": dec_ms * 1e3, "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
+                "append_us": (prof["append_ms"] / prof["append_launches"] * 1e3) if prof["append_launches"] else None,
                 "copy_kernel_gbs": r["copy_gbs"],
                 "timing": "kernel events from a second pass over the same K steps"}
     cb = None if (args.no_cpu_baseline or args.quick) else cpu_baseline(w, r["mode"])
-    # library kernels per timed step: decode + merge (+ append); the L2 flush is a torch fill
-    launches = prof["decode_launches"] + prof["merge_launches"] + (args.steps if w.append_steps else 0)
+    # library kernels in the timed steps: decode + merge + append; the L2 flush is a torch fill
+    launches = prof["decode_launches"] + prof["merge_launches"] + prof["append_launches"]
     ms = r["ms_all"]
     line = {
         "metric": METRIC, "value": tbps, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -139,6 +139,22 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
                           int page_size, int num_total_pages, int num_indices, pd_dtype dtype,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Append to a contiguous cache (batch_paged_decode.rs, module doc "Companion
+ * plans": KvCacheAppendPlan, the append to a rank-4 cache with no page
+ * table). For every request b and kv head h, row `position` of
+ * k_cache[b, h, :, :] becomes k_new[b, h, :], bit for bit; the same for v.
+ * With the cache holding `position` valid rows before the call, a decode
+ * with valid_kv_len = position + 1 then sees the new token last.
+ *
+ * k_new, v_new: device [batch, num_kv_heads, head_dim] T, 16-byte aligned.
+ * k_cache, v_cache: device [batch, num_kv_heads, max_kv_len, head_dim] T,
+ *   modified in place. 0 <= position < max_kv_len (PD_ERR_INVALID otherwise).
+ */
+pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
+                               int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
+                               void* stream);
+
 /* Workspace bytes pd_contiguous_decode needs (same rules as above). */
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads,
                                             int head_dim, pd_dtype dtype);
@@ -197,15 +213,16 @@ pd_status pd_read_device_flags(const void* workspace, int32_t* flags, void* stre
 pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream);
 
 /*
- * Kernel timing for measurement. While enabled, every decode call records
- * CUDA events on its stream around its decode kernel and its merge kernel.
- * pd_profile_read() synchronizes on those events, returns the summed
- * milliseconds and launch counts since the last read, and starts a new
- * count. Enabling costs two event records per kernel; it is off by default.
+ * Kernel timing for measurement. While enabled, every call records CUDA
+ * events on its stream around each kernel it launches (decode, merge,
+ * append). pd_profile_read() synchronizes on those events, returns the
+ * summed milliseconds and launch counts per kind since the last read (host
+ * pointers; any may be NULL), and starts a new count. Enabling costs two
+ * event records per kernel; it is off by default.
  */
 pd_status pd_profile_enable(int enable);
 pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms,
-                          int* merge_launches);
+                          int* merge_launches, double* append_ms, int* append_launches);
 
 /*
  * pd_paged_decode for callers that cannot allocate device memory at call

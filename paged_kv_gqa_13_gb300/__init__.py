@@ -48,7 +48,9 @@ _SIGS = {
     "pd_copy_bytes": (_I, [_P, _P, _S, _P]),
     "pd_profile_enable": (_I, [_I]),
     "pd_profile_read": (_I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
+                             ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+    "pd_contiguous_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pd_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pd_last_error_string": (ctypes.c_char_p, []),
     "pd_version": (_I, []),
@@ -206,7 +208,17 @@ def pd_profile_enable(enable: bool = True) -> None:
 
 
 def pd_profile_read() -> dict:
-    dm, mm = ctypes.c_double(0), ctypes.c_double(0)
-    dn, mn = ctypes.c_int(0), ctypes.c_int(0)
-    _check(_lib.pd_profile_read(ctypes.byref(dm), ctypes.byref(dn), ctypes.byref(mm), ctypes.byref(mn)))
-    return {"decode_ms": dm.value, "decode_launches": dn.value, "merge_ms": mm.value, "merge_launches": mn.value}
+    dm, mm, am = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    dn, mn, an = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.pd_profile_read(ctypes.byref(dm), ctypes.byref(dn), ctypes.byref(mm), ctypes.byref(mn),
+                                ctypes.byref(am), ctypes.byref(an)))
+    return {"decode_ms": dm.value, "decode_launches": dn.value, "merge_ms": mm.value, "merge_launches": mn.value,
+            "append_ms": am.value, "append_launches": an.value}
+
+
+def pd_contiguous_append(k_new, v_new, k_cache, v_cache, position: int, stream=None) -> None:
+    """k_new, v_new [batch, Hk, D] into row `position` of k_cache, v_cache [batch, Hk, max_kv_len, D]."""
+    batch, num_kv_heads, head_dim = k_new.shape
+    max_kv_len = k_cache.shape[2]
+    _check(_lib.pd_contiguous_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), batch, num_kv_heads,
+                                     head_dim, max_kv_len, int(position), _dtype_code(k_new), _stream(stream)))

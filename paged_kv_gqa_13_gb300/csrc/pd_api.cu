@@ -235,6 +235,7 @@ struct Profile {
     std::vector<cudaEvent_t> free_events;
     std::vector<cudaEvent_t> decode_marks;  // pairs: start, end
     std::vector<cudaEvent_t> merge_marks;
+    std::vector<cudaEvent_t> append_marks;
 };
 Profile g_prof;
 std::mutex g_prof_mu;
@@ -355,6 +356,22 @@ __global__ void __launch_bounds__(128) append_kernel(const uint8_t* k_new, const
     for (int off = lane * 16; off < row_bytes; off += 32 * 16) {
         *reinterpret_cast<uint4*>(k_data + dst + off) = __ldg(reinterpret_cast<const uint4*>(k_new + src + off));
         *reinterpret_cast<uint4*>(v_data + dst + off) = __ldg(reinterpret_cast<const uint4*>(v_new + src + off));
+    }
+}
+
+// One warp per (request, kv head): copy the new K and V rows into row
+// `position` of the contiguous cache.
+__global__ void __launch_bounds__(128) contiguous_append_kernel(const uint8_t* k_new, const uint8_t* v_new,
+                                                                uint8_t* k_cache, uint8_t* v_cache, int batch, int Hk,
+                                                                int row_bytes, long long max_kv_len, int position) {
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (w >= (long long)batch * Hk) return;
+    const size_t dst = (size_t(w) * size_t(max_kv_len) + size_t(position)) * size_t(row_bytes);
+    const size_t src = size_t(w) * size_t(row_bytes);
+    for (int off = lane * 16; off < row_bytes; off += 32 * 16) {
+        *reinterpret_cast<uint4*>(k_cache + dst + off) = __ldg(reinterpret_cast<const uint4*>(k_new + src + off));
+        *reinterpret_cast<uint4*>(v_cache + dst + off) = __ldg(reinterpret_cast<const uint4*>(v_new + src + off));
     }
 }
 
@@ -528,12 +545,45 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
     pd_status st = check_workspace(workspace, workspace_bytes, PD_WORKSPACE_HEADER_BYTES);
     if (st != PD_OK) return st;
     const long long warps = (long long)batch * num_kv_heads;
+    std::unique_lock<std::mutex> plk(g_prof_mu);
+    const bool prof = g_prof.on;
+    if (!prof) plk.unlock();
+    if (prof) mark(&g_prof.append_marks, static_cast<cudaStream_t>(stream));
     append_kernel<<<unsigned((warps + 3) / 4), 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), static_cast<uint8_t*>(k_data),
         static_cast<uint8_t*>(v_data), indices, indptr, last_page_len, batch, num_kv_heads,
         int(head_dim * elem_size(dtype)), page_size, num_total_pages, num_indices, static_cast<int*>(workspace));
     cudaError_t e = cudaGetLastError();
+    if (prof) mark(&g_prof.append_marks, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return ok();
+}
+
+pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
+                               int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
+                               void* stream) {
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
+    if (batch <= 0 || num_kv_heads <= 0 || max_kv_len <= 0)
+        return fail(PD_ERR_INVALID, "batch, num_kv_heads and max_kv_len must be positive");
+    if (position < 0 || position >= max_kv_len)
+        return fail(PD_ERR_INVALID, "position (%d) must be in [0, max_kv_len=%d)", position, max_kv_len);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!k_new || !v_new || !k_cache || !v_cache) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(PD_ERR_UNSUPPORTED, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::unique_lock<std::mutex> plk(g_prof_mu);
+    const bool prof = g_prof.on;
+    if (!prof) plk.unlock();
+    if (prof) mark(&g_prof.append_marks, s);
+    const long long warps = (long long)batch * num_kv_heads;
+    contiguous_append_kernel<<<unsigned((warps + 3) / 4), 128, 0, s>>>(
+        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), static_cast<uint8_t*>(k_cache),
+        static_cast<uint8_t*>(v_cache), batch, num_kv_heads, int(head_dim * elem_size(dtype)), max_kv_len, position);
+    cudaError_t e = cudaGetLastError();
+    if (prof) mark(&g_prof.append_marks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "contiguous append launch");
     return ok();
 }
 
@@ -597,7 +647,8 @@ pd_status pd_profile_enable(int enable) {
     return ok();
 }
 
-pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms, int* merge_launches) {
+pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms, int* merge_launches,
+                          double* append_ms, int* append_launches) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     auto sum = [](std::vector<cudaEvent_t>& v, double* ms, int* n) -> cudaError_t {
         double t = 0;
@@ -619,8 +670,10 @@ pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge
     };
     cudaError_t e1 = sum(g_prof.decode_marks, decode_ms, decode_launches);
     cudaError_t e2 = sum(g_prof.merge_marks, merge_ms, merge_launches);
+    cudaError_t e3 = sum(g_prof.append_marks, append_ms, append_launches);
     if (e1 != cudaSuccess) return cuda_fail(e1, "reading decode events");
     if (e2 != cudaSuccess) return cuda_fail(e2, "reading merge events");
+    if (e3 != cudaSuccess) return cuda_fail(e3, "reading append events");
     return ok();
 }
 

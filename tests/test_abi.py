@@ -83,6 +83,11 @@ def test_contiguous_and_append_and_merge_reject_bad_arguments():
                              0, None) == pd.PD_ERR_WORKSPACE
     assert L.pd_paged_append(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 16, 10, 4, pd.PD_F16, FAKE,
                              16, None) == pd.PD_ERR_WORKSPACE
+    # contiguous append: position outside [0, max_kv_len), bad head_dim, null cache
+    assert L.pd_contiguous_append(FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 40, 40, pd.PD_F16, None) == pd.PD_ERR_INVALID
+    assert L.pd_contiguous_append(FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 40, -1, pd.PD_F16, None) == pd.PD_ERR_INVALID
+    assert L.pd_contiguous_append(FAKE, FAKE, FAKE, FAKE, 2, 2, 96, 40, 3, pd.PD_F16, None) == pd.PD_ERR_UNSUPPORTED
+    assert L.pd_contiguous_append(FAKE, FAKE, None, FAKE, 2, 2, 128, 40, 3, pd.PD_F16, None) == pd.PD_ERR_INVALID
     assert L.pd_merge_states(FAKE, FAKE, 0, 4, 128, FAKE, None, pd.PD_F32, None) == pd.PD_ERR_INVALID
     assert L.pd_merge_states(FAKE, FAKE, 2, 4, 100, FAKE, None, pd.PD_F32, None) == pd.PD_ERR_UNSUPPORTED
     assert L.pd_copy_bytes(FAKE, FAKE, 10, None) == pd.PD_ERR_UNSUPPORTED

@@ -75,3 +75,56 @@ def test_append_flags_bad_tables():
     # in the second call request 0 (good) was written and request 1 was not
     changed = (dw.k.view(torch.int16) != before.view(torch.int16)).any(dim=-1).nonzero()
     assert len(changed) == w.num_kv_heads
+
+
+# --- contiguous cache ----------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,Hq,Hk,D,L", [("f16", 32, 8, 128, 300), ("bf16", 64, 8, 128, 97),
+                                             ("f32", 8, 8, 64, 40), ("bf16", 16, 4, 256, 65)])
+def test_contiguous_append_then_decode(dtype, Hq, Hk, D, L):
+    """Each step writes row n of every (request, kv head), bit for bit as the
+    oracle does, and a decode over n + 1 rows then matches the oracle."""
+    import math
+
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    B, n0, steps = 3, L - 4, 4
+    seed = 150 + L
+    kc = wl.normal((B, Hk, L, D), dtype, wl.stream_key(seed, "k"))
+    vc = wl.normal((B, Hk, L, D), dtype, wl.stream_key(seed, "v"))
+    nan = wl.nan_value(dtype)
+    kc[:, :, n0:] = nan
+    vc[:, :, n0:] = nan
+    q = wl.normal((B, Hq, D), dtype, wl.stream_key(seed, "q"))
+    scale = float(np.float32(1 / math.sqrt(D)))
+    kd, vd, qd = to_dev(kc, dtype), to_dev(vc, dtype), to_dev(q, dtype)
+    o = torch.empty_like(qd)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    code = {"f32": pd.PD_F32, "f16": pd.PD_F16, "bf16": pd.PD_BF16}[dtype]
+    ws = pd.alloc_workspace(pd.pd_contiguous_decode_workspace_bytes(B, Hq, Hk, D, code))
+    bits = np.uint32 if dtype == "f32" else np.uint16
+    for step in range(steps):
+        n = n0 + step
+        kn = wl.normal((B, Hk, D), dtype, wl.stream_key(seed + step, "k_new"))
+        vn = wl.normal((B, Hk, D), dtype, wl.stream_key(seed + step, "v_new"))
+        pd.pd_contiguous_append(to_dev(kn, dtype), to_dev(vn, dtype), kd, vd, n)
+        oracle.contiguous_append(kn, vn, kc, vc, n, dtype)
+        assert np.array_equal(to_host_raw(kd, dtype).view(bits), kc.view(bits)), f"K differs, step {step}"
+        assert np.array_equal(to_host_raw(vd, dtype).view(bits), vc.view(bits)), f"V differs, step {step}"
+        pd.pd_contiguous_decode(qd, kd, vd, o, lse, n + 1, scale, ws)
+        compare(o, lse, *oracle.contiguous_decode(q, kc, vc, Hq, n + 1, scale, dtype), dtype, f"step {step}")
+    assert pd.pd_read_device_flags(ws) == 0
+
+
+def test_contiguous_append_rejects_position_past_the_cache():
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    kn = torch.zeros(2, 2, 64, dtype=torch.float16, device="cuda")
+    kc = torch.zeros(2, 2, 10, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(pd.PagedecodeError):
+        pd.pd_contiguous_append(kn, kn, kc, kc, 10)
+    assert torch.all(kc == 0)
