@@ -218,6 +218,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                 j = i % w.append_steps
                 ind, ptr, lpl = dev_tables[j]
                 kn, vn = appends[j]
+                if args.append == "fused":
+                    pd.pd_paged_append_decode(q, kn, vn, k, v, ind, ptr, lpl, o, lse, w.sm_scale, ws)
+                    return
                 pd.pd_paged_append(kn, vn, k, v, ind, ptr, lpl, ws)
             else:
                 ind, ptr, lpl = dev_tables[0]
@@ -227,6 +230,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         if w.append_steps:
             ab = 2 * w.batch * w.num_kv_heads * w.head_dim * wl.ELEM_BYTES[w.dtype] * 2
             bytes_per_step = [b + ab for b in bytes_per_step]
+            if args.append == "fused":  # the one kernel also moves the appended rows
+                decode_bytes_per_step = bytes_per_step
 
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
@@ -408,6 +413,8 @@ def main():
                     choices=["tiny", "llama3_8b", "long_context", "long_context_contiguous", "ragged_70b",
                              "mha_append"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--append", default="fused", choices=["fused", "separate"],
+                    help="append workloads: one fused append + decode launch, or an append launch then a decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="decode steps only: no copy-peak, end-to-end or CPU-baseline legs (for profiler runs)")
@@ -468,7 +475,8 @@ def main():
         "metric": METRIC, "value": tbps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "mode": r["mode"], "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+        "config": {"workload": w.name, "mode": r["mode"] + (f", append {args.append}" if w.append_steps else ""),
+                   "batch": w.batch, "num_qo_heads": w.num_qo_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
                    "kv_tokens": int(w.table.kv_len().sum()), "bytes_per_step": int(r["bytes_mean"]),
                    "l2": "flushed before every timed step, outside the timed events: 512 MB written, then "

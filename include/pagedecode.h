@@ -140,6 +140,33 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Append, then decode, in one kernel launch. The companion plans of
+ * batch_paged_decode.rs (module doc "Companion plans": PagedKvAppendPlan, then
+ * BatchPagedDecodePlan) run as two plans per decode step; this call gives
+ * exactly the result of pd_paged_append followed by pd_paged_decode on the
+ * same arguments. That is, the K/V pool after the call is bit for bit the one
+ * pd_paged_append leaves, and o / lse are those pd_paged_decode returns on it.
+ *
+ * Each decode warp whose chunk holds a request's new row (row
+ * last_page_len[b] - 1 of its last page) first stores that row, then reads
+ * the chunk. No other launch is made for the append, and no grid-wide barrier
+ * is taken.
+ *
+ * Arguments are those of pd_paged_decode plus k_new, v_new (device
+ * [batch, num_kv_heads, head_dim] T, 16-byte aligned); k_data and v_data are
+ * modified in place, and the table must already describe the new token (as for
+ * pd_paged_append). A request with no page, a bad last page id or a
+ * last_page_len outside [1, page_size] is not appended to and is flagged in
+ * the status word; the decode of the other requests is unaffected.
+ */
+pd_status pd_paged_append_decode(const void* q, const void* k_new, const void* v_new, void* k_data,
+                                 void* v_data, const int32_t* indices, const int32_t* indptr,
+                                 const int32_t* last_page_len, void* o, float* lse, int batch,
+                                 int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                                 int num_total_pages, int num_indices, float sm_scale, pd_dtype dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Append to a contiguous cache (batch_paged_decode.rs, module doc "Companion
  * plans": KvCacheAppendPlan, the append to a rank-4 cache with no page
  * table). For every request b and kv head h, row `position` of
@@ -154,6 +181,19 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
 pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
                                int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
                                void* stream);
+
+/*
+ * pd_contiguous_append at `position`, then pd_contiguous_decode with
+ * valid_kv_len = position + 1, in one launch (the contiguous-cache form of
+ * pd_paged_append_decode). 0 <= position < max_kv_len (PD_ERR_INVALID
+ * otherwise); k_cache, v_cache are modified in place; the workspace is that of
+ * pd_contiguous_decode.
+ */
+pd_status pd_contiguous_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                      void* v_cache, void* o, float* lse, int batch, int num_qo_heads,
+                                      int num_kv_heads, int head_dim, int max_kv_len, int position,
+                                      float sm_scale, pd_dtype dtype, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* Workspace bytes pd_contiguous_decode needs (same rules as above). */
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads,

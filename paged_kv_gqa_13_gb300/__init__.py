@@ -51,6 +51,9 @@ _SIGS = {
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "pd_contiguous_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pd_paged_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                    _P, _S, _P]),
+    "pd_contiguous_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "pd_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pd_last_error_string": (ctypes.c_char_p, []),
     "pd_version": (_I, []),
@@ -152,6 +155,29 @@ def pd_paged_decode(q, k_data, v_data, indices, indptr, last_page_len, o, lse, s
         _ptr(last_page_len), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
         num_total_pages, indices.numel(), float(sm_scale), _dtype_code(q), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+
+
+def pd_paged_append_decode(q, k_new, v_new, k_data, v_data, indices, indptr, last_page_len, o, lse,
+                           sm_scale: float, workspace, stream=None) -> None:
+    """pd_paged_append then pd_paged_decode in one launch; the table already holds the new token."""
+    batch, num_qo_heads, head_dim = q.shape
+    num_total_pages, num_kv_heads, page_size, _ = k_data.shape
+    _check(_lib.pd_paged_append_decode(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_data), _ptr(v_data), _ptr(indices) if indices.numel() else None,
+        _ptr(indptr), _ptr(last_page_len), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads, head_dim,
+        page_size, num_total_pages, indices.numel(), float(sm_scale), _dtype_code(q), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+
+
+def pd_contiguous_append_decode(q, k_new, v_new, k_cache, v_cache, o, lse, position: int, sm_scale: float,
+                                workspace, stream=None) -> None:
+    """pd_contiguous_append at `position`, then pd_contiguous_decode over position + 1 rows, in one launch."""
+    batch, num_qo_heads, head_dim = q.shape
+    _, num_kv_heads, max_kv_len, _ = k_cache.shape
+    _check(_lib.pd_contiguous_append_decode(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+        _ptr(lse) if lse is not None else None, batch, num_qo_heads, num_kv_heads, head_dim, max_kv_len,
+        int(position), float(sm_scale), _dtype_code(q), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def pd_paged_decode_noalloc(q, k_data, v_data, indices, indptr, last_page_len, o, lse, sm_scale: float,

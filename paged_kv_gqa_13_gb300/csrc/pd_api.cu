@@ -307,6 +307,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     m.pos_per_warp = a.pos_per_warp;
     m.contiguous = a.contiguous;
     m.npv = a.npv;
+    m.append = (a.k_new != nullptr && !a.contiguous) ? 1 : 0;
     const long long pairs = pl.segments * pl.heads_per_tile;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned((pairs + 3) / 4));
@@ -420,11 +421,13 @@ size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num
     return p.ws_bytes;
 }
 
-pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data, const int32_t* indices,
-                          const int32_t* indptr, const int32_t* last_page_len, void* o, float* lse, int batch,
-                          int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_total_pages,
-                          int num_indices, float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+// The paged decode, with the fused append when k_new / v_new are not null.
+static pd_status paged_decode_impl(const void* q, const void* k_new, const void* v_new, const void* k_data,
+                                   const void* v_data, const int32_t* indices, const int32_t* indptr,
+                                   const int32_t* last_page_len, void* o, float* lse, int batch, int num_qo_heads,
+                                   int num_kv_heads, int head_dim, int page_size, int num_total_pages,
+                                   int num_indices, float sm_scale, pd_dtype dtype, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0)
         return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads, page_size and num_total_pages must be positive");
@@ -471,12 +474,40 @@ pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data,
     a.q_scale = sm_scale * pd::kLog2e;
     a.contiguous = 0;
     a.slab_rows = page_size;
+    a.k_new = k_new;
+    a.v_new = v_new;
     return launch_decode(pl, a, head_dim, dtype, num_total_pages, static_cast<cudaStream_t>(stream));
 }
 
-pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int batch,
-                               int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
-                               float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data, const int32_t* indices,
+                          const int32_t* indptr, const int32_t* last_page_len, void* o, float* lse, int batch,
+                          int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_total_pages,
+                          int num_indices, float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    return paged_decode_impl(q, nullptr, nullptr, k_data, v_data, indices, indptr, last_page_len, o, lse, batch,
+                             num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale,
+                             dtype, workspace, workspace_bytes, stream);
+}
+
+pd_status pd_paged_append_decode(const void* q, const void* k_new, const void* v_new, void* k_data, void* v_data,
+                                 const int32_t* indices, const int32_t* indptr, const int32_t* last_page_len, void* o,
+                                 float* lse, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int num_total_pages, int num_indices, float sm_scale, pd_dtype dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_new || !v_new) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(PD_ERR_UNSUPPORTED, "k_new and v_new must be 16-byte aligned");
+    return paged_decode_impl(q, k_new, v_new, k_data, v_data, indices, indptr, last_page_len, o, lse, batch,
+                             num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale,
+                             dtype, workspace, workspace_bytes, stream);
+}
+
+// The contiguous decode, with the fused append of row valid_kv_len - 1 when
+// k_new / v_new are not null.
+static pd_status contiguous_decode_impl(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                        const void* v_cache, void* o, float* lse, int batch, int num_qo_heads,
+                                        int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
+                                        float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || max_kv_len <= 0)
         return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads and max_kv_len must be positive");
@@ -526,7 +557,30 @@ pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v
     a.valid_kv_len = valid_kv_len;
     a.vpage = vpage;
     a.npv = npv;
+    a.k_new = k_new;
+    a.v_new = v_new;
     return launch_decode(pl, a, head_dim, dtype, batch, static_cast<cudaStream_t>(stream));
+}
+
+pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int batch,
+                               int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
+                               float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return contiguous_decode_impl(q, nullptr, nullptr, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
+                                  head_dim, max_kv_len, valid_kv_len, sm_scale, dtype, workspace, workspace_bytes,
+                                  stream);
+}
+
+pd_status pd_contiguous_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                      void* v_cache, void* o, float* lse, int batch, int num_qo_heads,
+                                      int num_kv_heads, int head_dim, int max_kv_len, int position, float sm_scale,
+                                      pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_new || !v_new) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(PD_ERR_UNSUPPORTED, "k_new and v_new must be 16-byte aligned");
+    if (position < 0 || position >= max_kv_len)
+        return fail(PD_ERR_INVALID, "position (%d) must be in [0, max_kv_len=%d)", position, max_kv_len);
+    return contiguous_decode_impl(q, k_new, v_new, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
+                                  head_dim, max_kv_len, position + 1, sm_scale, dtype, workspace, workspace_bytes,
+                                  stream);
 }
 
 pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, void* v_data, const int32_t* indices,

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         const bool have = walk.next<kRC>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
+        if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
         if (lane != 0) return;
         if (!have) {
             meta[slot] = make_int4(0, kEndOfWork, 0, 0);

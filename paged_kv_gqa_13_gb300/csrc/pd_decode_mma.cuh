@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(256, 1)
         const bool have = walk.next<kMmaRows>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
+        if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
         if (lane != 0) return;
         if (!have) {
             meta[slot] = make_int4(0, kEndOfWork, 0, 0);

@@ -44,6 +44,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy global stores before async-proxy
+// (bulk copy / TMA) reads issued after it (and after a warp barrier, by
+// another lane of the warp).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -351,6 +358,11 @@ struct DecodeArgs {
     long long slab_rows;       // rows from one (page | request, kv head) slab to the next:
                                // page_size (paged) or max_kv_len (contiguous)
     int valid_kv_len, vpage, npv;  // contiguous: valid rows, rows per virtual page, pages per request
+    // Fused append (null otherwise): [batch, num_kv_heads, D] rows that become
+    // the last valid row of every (request, kv head) before it is read. The
+    // kernel then writes into k and v.
+    const void* k_new;
+    const void* v_new;
 };
 
 struct MergeArgs {
@@ -364,6 +376,7 @@ struct MergeArgs {
     int n_pos;
     long long pos_per_warp;
     int contiguous, npv;
+    int append;  // fused append: a request with no page is an error (flagged)
 };
 
 // Position range [lo, hi) of request b within one pass over the positions.

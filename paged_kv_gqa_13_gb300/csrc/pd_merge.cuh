@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(128, 1) merge_partials_kernel(const MergeArgs 
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     float L = kNegInf;
+    if (a.append && hi <= lo && sh == 0 && h == 0 && lane == 0) atomicOr(a.flags, kFlagBadIndptr);
     if (hi > lo) {
         const long long first = ((long long)sh * a.n_pos + lo) / a.pos_per_warp;
         const long long last = ((long long)sh * a.n_pos + hi - 1) / a.pos_per_warp;

@@ -21,8 +21,10 @@ namespace pd {
 
 constexpr int kTableMax = 512;  // requests whose indptr / last_page_len are staged in smem
 
-// Chunk metadata flags.
-constexpr int kSegStart = 1, kSegEnd = 2, kSegComplete = 4, kEndOfWork = 8;
+// Chunk metadata flags. kAppendRow marks the chunk whose last row is the
+// request's new row in a fused append + decode.
+constexpr int kSegStart = 1, kSegEnd = 2, kSegComplete = 4, kEndOfWork = 8, kAppendRow = 16;
+constexpr int kKhShift = 5;  // e_khf = kv head << kKhShift | flags
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -54,7 +56,7 @@ struct Walk {
     unsigned mask;  // lanes whose position belongs to a request
     int cur, j;     // lane being emitted, chunk within its position
     int nxt;        // prefetched page id of position wbase + 32 + lane
-    int e_slab, e_row, e_khf, e_valid, e_qrow, e_seg;  // e_khf = kh << 4 | flags
+    int e_slab, e_row, e_khf, e_valid, e_qrow, e_seg;  // e_khf = kh << kKhShift | flags
 
     __device__ __forceinline__ Walk(const DecodeArgs& args, const int* si, const int* sl, long long p0_,
                                     long long pend_, int lane_)
@@ -114,24 +116,33 @@ struct Walk {
             if (b < a.batch && i >= lo && i < hi) {
                 has = true;
                 const int kh = sh / a.head_tiles, ht = sh % a.head_tiles;
+                const bool last = i == hi - 1;
+                int fl = 0;
                 if (contiguous) {
-                    e_valid = (i == hi - 1) ? last_len(b) : a.vpage;
+                    e_valid = last ? last_len(b) : a.vpage;
                     e_slab = b;
                     e_row = (i - lo) * a.vpage;
+                    if (last && a.k_new != nullptr && e_valid > 0) fl |= kAppendRow;
                 } else {
-                    e_valid = (i == hi - 1) ? last_len(b) : a.page_size;
+                    e_valid = last ? last_len(b) : a.page_size;
                     if (pg < 0 || pg >= a.num_total_pages) {
                         atomicOr(a.flags, kFlagBadPage);
                         e_valid = 0;
                         pg = 0;
                     }
                     e_slab = pg;
+                    if (last && a.k_new != nullptr) {
+                        // The new row goes to row last_page_len - 1; a length
+                        // outside [1, page_size] or a bad page id skips it.
+                        const int raw = staged ? s_lpl[b] : __ldg(a.last_page_len + b);
+                        if (raw == 0) atomicOr(a.flags, kFlagBadLastPageLen);
+                        if (e_valid > 0 && raw >= 1 && raw <= a.page_size) fl |= kAppendRow;
+                    }
                 }
-                int fl = 0;
                 if (i == lo || p == p0) fl |= kSegStart;
                 if (i == hi - 1 || p == pend - 1) fl |= kSegEnd;
                 if ((long long)sh * N + lo >= p0 && (long long)sh * N + hi <= pend) fl |= kSegComplete;
-                e_khf = (kh << 4) | fl;
+                e_khf = (kh << kKhShift) | fl;
                 e_qrow = b * a.num_qo_heads + kh * a.group + ht * a.heads_per_tile;
                 e_seg = sh * a.batch + b;
             }
@@ -226,13 +237,13 @@ struct Walk {
         ck->row0 = __shfl_sync(kFull, e_row, cur) + j * CR;
         ck->qrow = __shfl_sync(kFull, e_qrow, cur);
         ck->seg = __shfl_sync(kFull, e_seg, cur);
-        ck->kh = khf >> 4;
+        ck->kh = khf >> kKhShift;
         const int nck = valid > CR ? (valid + CR - 1) / CR : 1;
         int rows = valid - j * CR;
         ck->rows = rows < 0 ? 0 : (rows > CR ? CR : rows);
         int flags = khf & kSegComplete;
         if (j == 0) flags |= khf & kSegStart;
-        if (j == nck - 1) flags |= khf & kSegEnd;
+        if (j == nck - 1) flags |= khf & (kSegEnd | kAppendRow);
         ck->flags = flags;
         if (++j == nck) {
             j = 0;
@@ -241,5 +252,27 @@ struct Walk {
         return true;
     }
 };
+
+// Fused append: the whole warp writes request b's new K and V rows for kv
+// head ck.kh into the chunk's last row (row ck.row0 + ck.rows - 1 of its
+// slab), then fences them so that the chunk's copy, issued afterwards by
+// lane 0, reads them. Every warp whose chunk holds the row writes it (the same
+// bytes), so no warp depends on another's store.
+__device__ __forceinline__ void write_new_row(const DecodeArgs& a, const Chunk& ck, int lane, size_t row_bytes) {
+    const int b = ck.seg % a.batch;
+    const size_t src = (size_t(b) * a.num_kv_heads + ck.kh) * row_bytes;
+    const size_t dst =
+        ((size_t(ck.slab) * a.num_kv_heads + ck.kh) * size_t(a.slab_rows) + size_t(ck.row0 + ck.rows - 1)) * row_bytes;
+    uint8_t* kd = static_cast<uint8_t*>(const_cast<void*>(a.k)) + dst;
+    uint8_t* vd = static_cast<uint8_t*>(const_cast<void*>(a.v)) + dst;
+    const uint8_t* ks = static_cast<const uint8_t*>(a.k_new) + src;
+    const uint8_t* vs = static_cast<const uint8_t*>(a.v_new) + src;
+    for (size_t off = size_t(lane) * 16; off < row_bytes; off += 32 * 16) {
+        *reinterpret_cast<uint4*>(kd + off) = __ldg(reinterpret_cast<const uint4*>(ks + off));
+        *reinterpret_cast<uint4*>(vd + off) = __ldg(reinterpret_cast<const uint4*>(vs + off));
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+}
 
 }  // namespace pd
