@@ -17,6 +17,9 @@ namespace pd {
 bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks);
 bool lookup_kernels_f16(int head_dim, int heads, KernelSet* ks);
 bool lookup_kernels_bf16(int head_dim, int heads, KernelSet* ks);
+bool lookup_fused_f32(int head_dim, int heads, const void** fn);
+bool lookup_fused_f16(int head_dim, int heads, const void** fn);
+bool lookup_fused_bf16(int head_dim, int heads, const void** fn);
 }  // namespace pd
 
 namespace {
@@ -47,9 +50,9 @@ size_t elem_size(pd_dtype dt) { return dt == PD_F32 ? 4 : 2; }
 
 bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
     switch (dt) {
-        case PD_F32: return pd::lookup_kernels_f32(D, G, ks);
-        case PD_F16: return pd::lookup_kernels_f16(D, G, ks);
-        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks);
+        case PD_F32: return pd::lookup_kernels_f32(D, G, ks) && pd::lookup_fused_f32(D, G, &ks->decode_fused);
+        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fused_f16(D, G, &ks->decode_fused);
+        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fused_bf16(D, G, &ks->decode_fused);
     }
     return false;
 }
@@ -176,9 +179,14 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
     p->smem = size_t(p->ks.smem_slack) + size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
     if ((st = allow_smem(p->ks.decode, int(p->smem))) != PD_OK) return st;
-    int per_sm = 0;
+    if ((st = allow_smem(p->ks.decode_fused, int(p->smem))) != PD_OK) return st;
+    // One wave for either kernel: the lower of their occupancies.
+    int per_sm = 0, per_sm_fused = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->ks.decode, p->nwarps * 32, p->smem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_fused, p->ks.decode_fused, p->nwarps * 32, p->smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (per_sm_fused < per_sm) per_sm = per_sm_fused;
     if (per_sm < 1) per_sm = 1;
     p->ctas = di.sms * per_sm;
     p->total_warps = (long long)p->ctas * p->nwarps;
@@ -283,7 +291,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
         cfg.stream = stream;
         void* args[] = {&a, &maps[0], &maps[1]};
         if (prof) mark(&g_prof.decode_marks, stream);
-        e = cudaLaunchKernelExC(&cfg, pl.ks.decode, args);
+        e = cudaLaunchKernelExC(&cfg, a.k_new != nullptr ? pl.ks.decode_fused : pl.ks.decode, args);
         if (prof) mark(&g_prof.decode_marks, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     } else {

@@ -63,7 +63,8 @@ struct Cfg {
     static_assert(kRC >= kRW && kRC % (kRW * kRR) == 0, "rows per stage");
 };
 
-template <typename T, int D, int G>
+// kFused: also perform the fused append (a.k_new / a.v_new set).
+template <typename T, int D, int G, bool kFused>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     using C = Cfg<T, D, G>;
     using E = Elt<T>;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     const long long gwarp = (long long)blockIdx.x * nwarps + wid;
     const long long p0 = gwarp * a.pos_per_warp;
     const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
-    Walk walk(a, s_indptr, s_lpl, p0, pend, lane);
+    Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
 
@@ -116,10 +117,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot) {
         Chunk ck;
-        const bool have = walk.next<kRC>(&ck);
+        const bool have = walk.template next<kRC>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
-        if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+        if constexpr (kFused) {
+            if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+        }
         if (lane != 0) return;
         if (!have) {
             meta[slot] = make_int4(0, kEndOfWork, 0, 0);

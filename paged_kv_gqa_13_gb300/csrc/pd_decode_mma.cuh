@@ -63,7 +63,8 @@ __device__ __forceinline__ float2 unpack_pair(uint32_t w) {
     }
 }
 
-template <typename T, int D>
+// kFused: also perform the fused append (a.k_new / a.v_new set).
+template <typename T, int D, bool kFused>
 __global__ void __launch_bounds__(256, 1)
     decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using C = CfgMma<T, D>;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(256, 1)
     const long long gwarp = (long long)blockIdx.x * nwarps + wid;
     const long long p0 = gwarp * a.pos_per_warp;
     const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
-    Walk walk(a, s_indptr, s_lpl, p0, pend, lane);
+    Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
     if (lane == 0) {
@@ -114,10 +115,12 @@ __global__ void __launch_bounds__(256, 1)
     const size_t row_bytes = size_t(D) * sizeof(T);
     auto produce = [&](int slot) {
         Chunk ck;
-        const bool have = walk.next<kMmaRows>(&ck);
+        const bool have = walk.template next<kMmaRows>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
-        if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+        if constexpr (kFused) {
+            if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+        }
         if (lane != 0) return;
         if (!have) {
             meta[slot] = make_int4(0, kEndOfWork, 0, 0);

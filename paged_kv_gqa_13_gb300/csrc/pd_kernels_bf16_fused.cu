@@ -1,0 +1,6 @@
+// Fused append + decode kernels for element type __nv_bfloat16.
+#include "pd_kernels.cuh"
+
+namespace pd {
+bool lookup_fused_bf16(int head_dim, int heads, const void** fn) { return lookup_fused_t<__nv_bfloat16>(head_dim, heads, fn); }
+}  // namespace pd

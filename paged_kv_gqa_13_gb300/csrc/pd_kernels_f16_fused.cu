@@ -1,0 +1,6 @@
+// Fused append + decode kernels for element type __half.
+#include "pd_kernels.cuh"
+
+namespace pd {
+bool lookup_fused_f16(int head_dim, int heads, const void** fn) { return lookup_fused_t<__half>(head_dim, heads, fn); }
+}  // namespace pd

@@ -1,0 +1,6 @@
+// Fused append + decode kernels for element type float.
+#include "pd_kernels.cuh"
+
+namespace pd {
+bool lookup_fused_f32(int head_dim, int heads, const void** fn) { return lookup_fused_t<float>(head_dim, heads, fn); }
+}  // namespace pd

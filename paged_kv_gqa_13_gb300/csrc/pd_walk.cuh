@@ -43,6 +43,9 @@ struct Chunk {
     int seg;    // segment id: pass * batch + b
 };
 
+// kFused: the decode carries the fused append (DecodeArgs::k_new is set);
+// only then are new-row chunks marked.
+template <bool kFused>
 struct Walk {
     const DecodeArgs& a;
     const int* s_indptr;
@@ -122,7 +125,7 @@ struct Walk {
                     e_valid = last ? last_len(b) : a.vpage;
                     e_slab = b;
                     e_row = (i - lo) * a.vpage;
-                    if (last && a.k_new != nullptr && e_valid > 0) fl |= kAppendRow;
+                    if (kFused && last && e_valid > 0) fl |= kAppendRow;
                 } else {
                     e_valid = last ? last_len(b) : a.page_size;
                     if (pg < 0 || pg >= a.num_total_pages) {
@@ -131,7 +134,7 @@ struct Walk {
                         pg = 0;
                     }
                     e_slab = pg;
-                    if (last && a.k_new != nullptr) {
+                    if (kFused && last) {
                         // The new row goes to row last_page_len - 1; a length
                         // outside [1, page_size] or a bad page id skips it.
                         const int raw = staged ? s_lpl[b] : __ldg(a.last_page_len + b);
