@@ -52,10 +52,10 @@ def _lib():
         lib.oracle_paged_decode.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _L,
                                             ctypes.c_float, _I, _P, _P, _I]
         lib.oracle_contiguous_decode.argtypes = [_P, _P, _P, _I, _I, _I, _I, _L, _L, ctypes.c_float,
-                                                 _I, _P, _P, _I]
+                                                 _I, _I, _P, _P, _I]
         lib.oracle_paged_append.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]
         lib.oracle_merge_states.argtypes = [_P, _P, _I, _L, _I, _P, _P]
-        lib.oracle_contiguous_append.argtypes = [_P, _P, _P, _P, _I, _I, _I, _L, _L, _I]
+        lib.oracle_contiguous_append.argtypes = [_P, _P, _P, _P, _I, _I, _I, _L, _L, _I, _I]
         lib.oracle_round_to_dtype.argtypes = [_P, _L, _I, _P]
         for f in (lib.oracle_decode_elements, lib.oracle_paged_decode, lib.oracle_contiguous_decode,
                   lib.oracle_paged_append, lib.oracle_merge_states, lib.oracle_round_to_dtype,
@@ -117,16 +117,28 @@ def paged_decode_workload(w, table=None, threads: int = 0):
                         w.dtype, threads)
 
 
+LAYOUT_CODE = {"hnd": 0, "nhd": 1}
+
+
+def _contiguous_dims(cache, layout):
+    """(batch, num_kv_heads, max_kv_len, head_dim) of an HND [b, Hk, L, D] or NHD [b, L, Hk, D] cache."""
+    if layout == "hnd":
+        return cache.shape
+    batch, max_kv_len, num_kv_heads, head_dim = cache.shape
+    return batch, num_kv_heads, max_kv_len, head_dim
+
+
 def contiguous_decode(q, k_cache, v_cache, num_qo_heads, valid_kv_len, sm_scale, dtype,
-                      threads: int = 0):
-    """q [batch, Hq, D], k/v_cache [batch, Hk, max_kv_len, D]; returns float64 o, lse."""
+                      threads: int = 0, layout: str = "hnd"):
+    """q [batch, Hq, D], k/v_cache [batch, Hk, max_kv_len, D] (hnd) or [batch, max_kv_len, Hk, D]
+    (nhd); returns float64 o, lse."""
     q, k_cache, v_cache = _c(q), _c(k_cache), _c(v_cache)
-    batch, num_kv_heads, max_kv_len, head_dim = k_cache.shape
+    batch, num_kv_heads, max_kv_len, head_dim = _contiguous_dims(k_cache, layout)
     o = np.empty((batch, num_qo_heads, head_dim), dtype=np.float64)
     lse = np.empty((batch, num_qo_heads), dtype=np.float64)
     rc = _lib().oracle_contiguous_decode(q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
                                          batch, num_qo_heads, num_kv_heads, head_dim, max_kv_len,
-                                         valid_kv_len, float(sm_scale), DTYPE_CODE[dtype],
+                                         valid_kv_len, float(sm_scale), DTYPE_CODE[dtype], LAYOUT_CODE[layout],
                                          o.ctypes.data, lse.ctypes.data, threads)
     if rc:
         raise OracleError(f"oracle_contiguous_decode returned {rc}")
@@ -149,14 +161,14 @@ def paged_append(k_new, v_new, k_data, v_data, indices, indptr, last_page_len, d
         raise OracleError(f"oracle_paged_append returned {rc}")
 
 
-def contiguous_append(k_new, v_new, k_cache, v_cache, position, dtype):
-    """Write row `position` of every (request, kv head) of the host mirrors in place."""
+def contiguous_append(k_new, v_new, k_cache, v_cache, position, dtype, layout: str = "hnd"):
+    """Write token `position` of every (request, kv head) of the host mirrors in place."""
     k_new, v_new = _c(k_new), _c(v_new)
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
-    batch, num_kv_heads, max_kv_len, head_dim = k_cache.shape
+    batch, num_kv_heads, max_kv_len, head_dim = _contiguous_dims(k_cache, layout)
     rc = _lib().oracle_contiguous_append(k_new.ctypes.data, v_new.ctypes.data, k_cache.ctypes.data,
                                          v_cache.ctypes.data, batch, num_kv_heads, head_dim, max_kv_len,
-                                         int(position), DTYPE_CODE[dtype])
+                                         int(position), DTYPE_CODE[dtype], LAYOUT_CODE[layout])
     if rc:
         raise OracleError(f"oracle_contiguous_append returned {rc}")
 

@@ -197,16 +197,29 @@ int oracle_paged_decode(const void* q, const void* k_data, const void* v_data,
     return 0;
 }
 
+// Row index (in head_dim-element rows) of token t, kv head kh, request b in a
+// contiguous cache of one of two layouts:
+//   layout 0, HND: [batch, num_kv_heads, max_kv_len, head_dim] ([P1] decode_attention
+//                  k_cache [num_kv_heads, max_kv_len, head_dim], batch in front);
+//   layout 1, NHD: [batch, max_kv_len, num_kv_heads, head_dim] ([P2] gqa_decode:
+//                  token t of kv head kv_h starts at (t * n_kv_heads + kv_h) * head_dim,
+//                  batch in front).
+static size_t contiguous_row(int layout, int b, int kh, long t, int num_kv_heads, long max_kv_len) {
+    if (layout == 1 && ORACLE_MUTANT != 11)
+        return (size_t(b) * size_t(max_kv_len) + size_t(t)) * size_t(num_kv_heads) + size_t(kh);
+    return (size_t(b) * size_t(num_kv_heads) + size_t(kh)) * size_t(max_kv_len) + size_t(t);
+}
+
 // Decode over a contiguous cache, [P1] decode_attention arguments, with a batch
-// dimension in front: k_cache/v_cache [batch, num_kv_heads, max_kv_len, head_dim],
-// rows [0, valid_kv_len) valid for every request. A separate loop from the
-// paged walk on purpose: the two paths agreeing is itself a check.
+// dimension in front; rows [0, valid_kv_len) valid for every request; layout as
+// in contiguous_row. A separate loop from the paged walk on purpose: the two
+// paths agreeing is itself a check.
 int oracle_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, int batch,
                              int num_qo_heads, int num_kv_heads, int head_dim, long max_kv_len,
-                             long valid_kv_len, float sm_scale, int dtype, double* o_out,
+                             long valid_kv_len, float sm_scale, int dtype, int layout, double* o_out,
                              double* lse_out, int nthreads) {
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len <= 0 ||
-        valid_kv_len < 0 || valid_kv_len > max_kv_len || dtype < 0 || dtype > 2)
+        valid_kv_len < 0 || valid_kv_len > max_kv_len || dtype < 0 || dtype > 2 || layout < 0 || layout > 1)
         return 1;
     if (num_qo_heads % num_kv_heads != 0) return 1;
     const int group = num_qo_heads / num_kv_heads;
@@ -214,10 +227,13 @@ int oracle_contiguous_decode(const void* q, const void* k_cache, const void* v_c
     const double scale = double(sm_scale);
     parallel_for(long(batch) * num_qo_heads, nthreads, [&](long bh) {
         const int b = int(bh / num_qo_heads), h = int(bh % num_qo_heads);
-        const size_t base = (size_t(b) * num_kv_heads + size_t(h / group)) * size_t(max_kv_len);
+        const int kh = h / group;
+        auto addr = [&](long t, int d) {
+            return contiguous_row(layout, b, kh, t, num_kv_heads, max_kv_len) * size_t(head_dim) + size_t(d);
+        };
         attend(Q, size_t(bh) * head_dim, valid_kv_len, head_dim, scale,
-               [&](long t, int d) { return K.at((base + size_t(t)) * head_dim + size_t(d)); },
-               [&](long t, int d) { return V.at((base + size_t(t)) * head_dim + size_t(d)); },
+               [&](long t, int d) { return K.at(addr(t, d)); },
+               [&](long t, int d) { return V.at(addr(t, d)); },
                o_out + size_t(bh) * head_dim, lse_out + bh);
     });
     return 0;
@@ -253,19 +269,20 @@ int oracle_paged_append(const void* k_new, const void* v_new, void* k_data, void
 }
 
 // Append to a contiguous cache ([P3] "Companion plans": KvCacheAppendPlan, the
-// rank-4 cache with no page table): for every request b and kv head h, row
-// `position` of k_cache[b, h, :, :] becomes k_new[b, h, :], the same for v.
-// k_cache/v_cache [batch, num_kv_heads, max_kv_len, head_dim]. Returns 0 or 1.
+// rank-4 cache with no page table): for every request b and kv head h, token
+// `position` of kv head h of request b becomes k_new[b, h, :], the same for v.
+// Layout as in contiguous_row. Returns 0 or 1.
 int oracle_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
-                             int num_kv_heads, int head_dim, long max_kv_len, long position, int dtype) {
+                             int num_kv_heads, int head_dim, long max_kv_len, long position, int dtype,
+                             int layout) {
     if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_kv_len <= 0 || position < 0 ||
-        position >= max_kv_len || dtype < 0 || dtype > 2)
+        position >= max_kv_len || dtype < 0 || dtype > 2 || layout < 0 || layout > 1)
         return 1;
     const size_t row = size_t(head_dim) * elem_bytes(dtype);
     for (int b = 0; b < batch; ++b)
         for (int h = 0; h < num_kv_heads; ++h) {
             const long pos = ORACLE_MUTANT == 10 ? (position > 0 ? position - 1 : position + 1) : position;
-            const size_t dst = ((size_t(b) * num_kv_heads + h) * size_t(max_kv_len) + size_t(pos)) * row;
+            const size_t dst = contiguous_row(layout, b, h, pos, num_kv_heads, max_kv_len) * row;
             const size_t src = (size_t(b) * num_kv_heads + h) * row;
             std::memcpy(static_cast<uint8_t*>(k_cache) + dst, static_cast<const uint8_t*>(k_new) + src, row);
             std::memcpy(static_cast<uint8_t*>(v_cache) + dst, static_cast<const uint8_t*>(v_new) + src, row);

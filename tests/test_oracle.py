@@ -385,3 +385,61 @@ def test_contiguous_append_writes_the_new_last_row():
     np.testing.assert_allclose(o, oracle.decode_elements(vn, "f16"), rtol=0, atol=1e-6)
     with pytest.raises(oracle.OracleError):
         oracle.contiguous_append(kn, vn, kc, vc, L, "f16")
+
+
+def test_nhd_decode_reads_token_t_of_head_kh_at_the_page_offset():
+    # ferrox-cuda, src/attn.rs (gqa_decode): token t of kv head kv_h starts at
+    # element (t * n_kv_heads + kv_h) * head_dim. Plant one dominant key at
+    # token t0 of kv head 1, aligned with the query, and give every row of V
+    # its own flat offset as its value: the q heads of kv head 1 must return
+    # the V row at that offset, the others the mean of their V rows.
+    B, Hk, L, D, g, t0 = 2, 3, 7, 4, 2, 5
+    Hq = Hk * g
+    flat_k = np.zeros(B * L * Hk * D, dtype=np.float32)
+    flat_v = np.arange(B * L * Hk * D, dtype=np.float32) / D  # row r holds r, r + 1/D, ...
+    q = np.zeros((B, Hq, D), dtype=np.float32)
+    for b in range(B):
+        off = ((b * L + t0) * Hk + 1) * D
+        flat_k[off:off + D] = 8.0
+        q[b, 1 * g:2 * g, :] = 8.0
+    kc = flat_k.reshape(B, L, Hk, D)
+    vc = flat_v.reshape(B, L, Hk, D)
+    o, lse = oracle.contiguous_decode(q, kc, vc, Hq, L, 1.0, "f32", layout="nhd")
+    for b in range(B):
+        row = (b * L + t0) * Hk + 1
+        np.testing.assert_allclose(o[b, g:2 * g], np.tile(flat_v[row * D:(row + 1) * D], (g, 1)), atol=1e-9)
+        for kh in (0, 2):  # all scores 0: the plain mean of the kv head's rows
+            rows = [(b * L + t) * Hk + kh for t in range(L)]
+            mean = np.mean([flat_v[r * D:(r + 1) * D] for r in rows], axis=0)
+            np.testing.assert_allclose(o[b, kh * g], mean, atol=1e-12)
+            assert abs(lse[b, kh * g] - math.log(L)) < 1e-12
+
+
+def test_nhd_decode_equals_hnd_decode_of_the_transposed_cache():
+    # The layout changes only where a (token, head) row lives, never its value.
+    B, Hq, Hk, L, D, n = 2, 8, 2, 50, 64, 37
+    kc = wl.normal((B, L, Hk, D), "bf16", wl.stream_key(141, "k"))
+    vc = wl.normal((B, L, Hk, D), "bf16", wl.stream_key(141, "v"))
+    q = wl.normal((B, Hq, D), "bf16", wl.stream_key(141, "q"))
+    o1, l1 = oracle.contiguous_decode(q, kc, vc, Hq, n, 0.125, "bf16", layout="nhd")
+    o2, l2 = oracle.contiguous_decode(q, np.ascontiguousarray(kc.transpose(0, 2, 1, 3)),
+                                      np.ascontiguousarray(vc.transpose(0, 2, 1, 3)), Hq, n, 0.125, "bf16")
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_nhd_append_writes_token_position_of_every_head():
+    B, Hk, L, D, n = 2, 3, 9, 8, 6
+    kc = wl.normal((B, L, Hk, D), "f16", wl.stream_key(142, "k"))
+    vc = wl.normal((B, L, Hk, D), "f16", wl.stream_key(142, "v"))
+    kn = wl.normal((B, Hk, D), "f16", wl.stream_key(142, "k_new"))
+    vn = wl.normal((B, Hk, D), "f16", wl.stream_key(142, "v_new"))
+    kb, vb = kc.copy(), vc.copy()
+    oracle.contiguous_append(kn, vn, kc, vc, n, "f16", layout="nhd")
+    fk, fkb = kc.reshape(-1), kb.reshape(-1)
+    for b in range(B):
+        for h in range(Hk):
+            off = ((b * L + n) * Hk + h) * D  # the page's token-major offset
+            assert np.array_equal(fk[off:off + D], kn[b, h])
+            fkb[off:off + D] = kn[b, h]
+    assert np.array_equal(fk, fkb)  # nothing else changed
+    assert np.array_equal(vc[:, n], vn) and np.array_equal(np.delete(vc, n, axis=1), np.delete(vb, n, axis=1))

@@ -21,6 +21,7 @@ MUTANTS = {
     8: "append writes slot last_page_len instead of last_page_len - 1",
     9: "merge weights exp(L - lse_c) instead of exp(lse_c - L)",
     10: "contiguous append one row early",
+    11: "NHD cache addressed as HND",
 }
 
 
