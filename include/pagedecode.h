@@ -195,6 +195,28 @@ pd_status pd_contiguous_append_decode(const void* q, const void* k_new, const vo
                                       float sm_scale, pd_dtype dtype, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/*
+ * The token-major (NHD) contiguous cache. ferrox-cuda 0.15.2, src/attn.rs
+ * (gqa_decode) stores one sequence as [seq_len, n_kv_heads, head_dim]: token t
+ * of kv head h starts at element (t * n_kv_heads + h) * head_dim. These three
+ * calls take that layout with a batch dimension in front,
+ * k_cache / v_cache [batch, max_kv_len, num_kv_heads, head_dim], and are
+ * otherwise the calls of the same name without _nhd: the same arguments,
+ * results, workspace (pd_contiguous_decode_workspace_bytes) and errors.
+ */
+pd_status pd_contiguous_decode_nhd(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                   float* lse, int batch, int num_qo_heads, int num_kv_heads,
+                                   int head_dim, int max_kv_len, int valid_kv_len, float sm_scale,
+                                   pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+pd_status pd_contiguous_append_nhd(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                   int batch, int num_kv_heads, int head_dim, int max_kv_len,
+                                   int position, pd_dtype dtype, void* stream);
+pd_status pd_contiguous_append_decode_nhd(const void* q, const void* k_new, const void* v_new,
+                                          void* k_cache, void* v_cache, void* o, float* lse, int batch,
+                                          int num_qo_heads, int num_kv_heads, int head_dim,
+                                          int max_kv_len, int position, float sm_scale, pd_dtype dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes pd_contiguous_decode needs (same rules as above). */
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads,
                                             int head_dim, pd_dtype dtype);

@@ -54,6 +54,10 @@ _SIGS = {
     "pd_paged_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _P, _S, _P]),
     "pd_contiguous_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "pd_contiguous_decode_nhd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "pd_contiguous_append_nhd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pd_contiguous_append_decode_nhd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
+                                             _P]),
     "pd_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "pd_last_error_string": (ctypes.c_char_p, []),
     "pd_version": (_I, []),
@@ -248,3 +252,36 @@ def pd_contiguous_append(k_new, v_new, k_cache, v_cache, position: int, stream=N
     max_kv_len = k_cache.shape[2]
     _check(_lib.pd_contiguous_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), batch, num_kv_heads,
                                      head_dim, max_kv_len, int(position), _dtype_code(k_new), _stream(stream)))
+
+
+# --- token-major (NHD) contiguous cache: k_cache, v_cache [batch, max_kv_len, Hk, D] ----------
+
+def pd_contiguous_decode_nhd(q, k_cache, v_cache, o, lse, valid_kv_len: int, sm_scale: float, workspace,
+                             stream=None) -> None:
+    """pd_contiguous_decode on k_cache, v_cache [batch, max_kv_len, Hk, D]."""
+    batch, num_qo_heads, head_dim = q.shape
+    _, max_kv_len, num_kv_heads, _ = k_cache.shape
+    _check(_lib.pd_contiguous_decode_nhd(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads,
+        head_dim, max_kv_len, int(valid_kv_len), float(sm_scale), _dtype_code(q), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+
+
+def pd_contiguous_append_nhd(k_new, v_new, k_cache, v_cache, position: int, stream=None) -> None:
+    """k_new, v_new [batch, Hk, D] into token `position` of k_cache, v_cache [batch, max_kv_len, Hk, D]."""
+    batch, num_kv_heads, head_dim = k_new.shape
+    max_kv_len = k_cache.shape[1]
+    _check(_lib.pd_contiguous_append_nhd(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), batch,
+                                         num_kv_heads, head_dim, max_kv_len, int(position), _dtype_code(k_new),
+                                         _stream(stream)))
+
+
+def pd_contiguous_append_decode_nhd(q, k_new, v_new, k_cache, v_cache, o, lse, position: int, sm_scale: float,
+                                    workspace, stream=None) -> None:
+    """pd_contiguous_append_decode on k_cache, v_cache [batch, max_kv_len, Hk, D]."""
+    batch, num_qo_heads, head_dim = q.shape
+    _, max_kv_len, num_kv_heads, _ = k_cache.shape
+    _check(_lib.pd_contiguous_append_decode_nhd(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+        _ptr(lse) if lse is not None else None, batch, num_qo_heads, num_kv_heads, head_dim, max_kv_len,
+        int(position), float(sm_scale), _dtype_code(q), _ptr(workspace), workspace.numel(), _stream(stream)))

@@ -17,9 +17,14 @@ namespace pd {
 bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks);
 bool lookup_kernels_f16(int head_dim, int heads, KernelSet* ks);
 bool lookup_kernels_bf16(int head_dim, int heads, KernelSet* ks);
-bool lookup_fused_f32(int head_dim, int heads, const void** fn);
-bool lookup_fused_f16(int head_dim, int heads, const void** fn);
-bool lookup_fused_bf16(int head_dim, int heads, const void** fn);
+#define PD_VARIANTS(dt)                                                    \
+    bool lookup_fused_##dt(int head_dim, int heads, const void** fn);      \
+    bool lookup_nhd_##dt(int head_dim, int heads, const void** fn);        \
+    bool lookup_nhd_fused_##dt(int head_dim, int heads, const void** fn);
+PD_VARIANTS(f32)
+PD_VARIANTS(f16)
+PD_VARIANTS(bf16)
+#undef PD_VARIANTS
 }  // namespace pd
 
 namespace {
@@ -50,9 +55,15 @@ size_t elem_size(pd_dtype dt) { return dt == PD_F32 ? 4 : 2; }
 
 bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
     switch (dt) {
-        case PD_F32: return pd::lookup_kernels_f32(D, G, ks) && pd::lookup_fused_f32(D, G, &ks->decode_fused);
-        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fused_f16(D, G, &ks->decode_fused);
-        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fused_bf16(D, G, &ks->decode_fused);
+#define PD_LOOKUP(dt)                                                                                  \
+    if (!pd::lookup_kernels_##dt(D, G, ks)) return false;                                               \
+    ks->variant[0] = ks->decode;                                                                        \
+    return pd::lookup_fused_##dt(D, G, &ks->variant[1]) && pd::lookup_nhd_##dt(D, G, &ks->variant[2]) && \
+           pd::lookup_nhd_fused_##dt(D, G, &ks->variant[3]);
+        case PD_F32: { PD_LOOKUP(f32) }
+        case PD_F16: { PD_LOOKUP(f16) }
+        case PD_BF16: { PD_LOOKUP(bf16) }
+#undef PD_LOOKUP
     }
     return false;
 }
@@ -178,15 +189,16 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     if (p->nwarps > 8) p->nwarps = 8;
     if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
     p->smem = size_t(p->ks.smem_slack) + size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
-    if ((st = allow_smem(p->ks.decode, int(p->smem))) != PD_OK) return st;
-    if ((st = allow_smem(p->ks.decode_fused, int(p->smem))) != PD_OK) return st;
-    // One wave for either kernel: the lower of their occupancies.
-    int per_sm = 0, per_sm_fused = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->ks.decode, p->nwarps * 32, p->smem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_fused, p->ks.decode_fused, p->nwarps * 32, p->smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (per_sm_fused < per_sm) per_sm = per_sm_fused;
+    // The variants this plan may launch (NHD only on the contiguous cache) all
+    // share its layout; size one wave by the lowest of their occupancies.
+    int per_sm = 1 << 30;
+    for (int v = 0; v < (contiguous ? 4 : 2); ++v) {
+        if ((st = allow_smem(p->ks.variant[v], int(p->smem))) != PD_OK) return st;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, p->ks.variant[v], p->nwarps * 32, p->smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (n < per_sm) per_sm = n;
+    }
     if (per_sm < 1) per_sm = 1;
     p->ctas = di.sms * per_sm;
     p->total_warps = (long long)p->ctas * p->nwarps;
@@ -216,17 +228,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K or V as a 4-D tensor {head_dim, slab_rows, kv heads, slabs} of 16-bit
-// elements, read in boxes of 64 columns x 16 rows with the 128-byte swizzle;
-// rows outside the tensor read as zero.
+// K or V as a 4-D tensor of 16-bit elements, {head_dim, slab_rows, kv heads,
+// slabs} (HND) or {head_dim, kv heads, slab_rows, slabs} (NHD), read in boxes
+// of 64 columns x 16 rows of one kv head with the 128-byte swizzle; rows
+// outside the tensor read as zero. Either way a box lands as 16 rows of 128
+// bytes.
 pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long slab_rows, int Hk,
-                      long long slabs) {
+                      long long slabs, bool nhd) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(slab_rows), cuuint64_t(Hk), cuuint64_t(slabs)};
-    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(slab_rows) * D * 2,
-                                   cuuint64_t(Hk) * slab_rows * D * 2};
-    const cuuint32_t box[4] = {64, cuuint32_t(pd::kMmaRows), 1, 1};
+    const cuuint64_t row = cuuint64_t(D) * 2;
+    const cuuint64_t dims_hnd[4] = {cuuint64_t(D), cuuint64_t(slab_rows), cuuint64_t(Hk), cuuint64_t(slabs)};
+    const cuuint64_t dims_nhd[4] = {cuuint64_t(D), cuuint64_t(Hk), cuuint64_t(slab_rows), cuuint64_t(slabs)};
+    const cuuint64_t str_hnd[3] = {row, cuuint64_t(slab_rows) * row, cuuint64_t(Hk) * slab_rows * row};
+    const cuuint64_t str_nhd[3] = {row, cuuint64_t(Hk) * row, cuuint64_t(Hk) * slab_rows * row};
+    const cuuint64_t* dims = nhd ? dims_nhd : dims_hnd;
+    const cuuint64_t* strides = nhd ? str_nhd : str_hnd;
+    const cuuint32_t box_hnd[4] = {64, cuuint32_t(pd::kMmaRows), 1, 1};
+    const cuuint32_t box_nhd[4] = {64, 1, cuuint32_t(pd::kMmaRows), 1};
+    const cuuint32_t* box = nhd ? box_nhd : box_hnd;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = enc(map, dt == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -269,11 +289,14 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 
 // ---------------------------------------------------------------- decode launch
 
-pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, cudaStream_t stream) {
+// nhd: the contiguous cache is token-major, [slabs, slab_rows, Hk, D].
+pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, bool nhd,
+                        cudaStream_t stream) {
+    const int variant = (a.k_new != nullptr ? pd::kVarFused : 0) | (nhd ? pd::kVarNhd : 0);
     CUtensorMap maps[2];
     if (pl.ks.tensor_maps && a.total_pos > 0) {
-        pd_status st = make_kv_map(&maps[0], a.k, dt, D, a.slab_rows, a.num_kv_heads, slabs);
-        if (st == PD_OK) st = make_kv_map(&maps[1], a.v, dt, D, a.slab_rows, a.num_kv_heads, slabs);
+        pd_status st = make_kv_map(&maps[0], a.k, dt, D, a.slab_rows, a.num_kv_heads, slabs, nhd);
+        if (st == PD_OK) st = make_kv_map(&maps[1], a.v, dt, D, a.slab_rows, a.num_kv_heads, slabs, nhd);
         if (st != PD_OK) return st;
     }
     std::unique_lock<std::mutex> plk(g_prof_mu);
@@ -291,7 +314,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
         cfg.stream = stream;
         void* args[] = {&a, &maps[0], &maps[1]};
         if (prof) mark(&g_prof.decode_marks, stream);
-        e = cudaLaunchKernelExC(&cfg, a.k_new != nullptr ? pl.ks.decode_fused : pl.ks.decode, args);
+        e = cudaLaunchKernelExC(&cfg, pl.ks.variant[variant], args);
         if (prof) mark(&g_prof.decode_marks, stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     } else {
@@ -368,15 +391,20 @@ __global__ void __launch_bounds__(128) append_kernel(const uint8_t* k_new, const
     }
 }
 
-// One warp per (request, kv head): copy the new K and V rows into row
-// `position` of the contiguous cache.
+// One warp per (request, kv head): copy the new K and V rows into token
+// `position` of the contiguous cache, HND [b, Hk, max_kv_len, D] or NHD
+// [b, max_kv_len, Hk, D].
 __global__ void __launch_bounds__(128) contiguous_append_kernel(const uint8_t* k_new, const uint8_t* v_new,
                                                                 uint8_t* k_cache, uint8_t* v_cache, int batch, int Hk,
-                                                                int row_bytes, long long max_kv_len, int position) {
+                                                                int row_bytes, long long max_kv_len, int position,
+                                                                int nhd) {
     const int lane = threadIdx.x & 31;
     const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (w >= (long long)batch * Hk) return;
-    const size_t dst = (size_t(w) * size_t(max_kv_len) + size_t(position)) * size_t(row_bytes);
+    const long long b = w / Hk, kh = w % Hk;
+    const size_t row = nhd ? (size_t(b) * size_t(max_kv_len) + size_t(position)) * size_t(Hk) + size_t(kh)
+                           : size_t(w) * size_t(max_kv_len) + size_t(position);
+    const size_t dst = row * size_t(row_bytes);
     const size_t src = size_t(w) * size_t(row_bytes);
     for (int off = lane * 16; off < row_bytes; off += 32 * 16) {
         *reinterpret_cast<uint4*>(k_cache + dst + off) = __ldg(reinterpret_cast<const uint4*>(k_new + src + off));
@@ -484,7 +512,7 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     a.slab_rows = page_size;
     a.k_new = k_new;
     a.v_new = v_new;
-    return launch_decode(pl, a, head_dim, dtype, num_total_pages, static_cast<cudaStream_t>(stream));
+    return launch_decode(pl, a, head_dim, dtype, num_total_pages, false, static_cast<cudaStream_t>(stream));
 }
 
 pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data, const int32_t* indices,
@@ -510,12 +538,12 @@ pd_status pd_paged_append_decode(const void* q, const void* k_new, const void* v
 }
 
 // The contiguous decode, with the fused append of row valid_kv_len - 1 when
-// k_new / v_new are not null.
+// k_new / v_new are not null; nhd: the cache is [batch, max_kv_len, Hk, D].
 static pd_status contiguous_decode_impl(const void* q, const void* k_new, const void* v_new, const void* k_cache,
                                         const void* v_cache, void* o, float* lse, int batch, int num_qo_heads,
                                         int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
                                         float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes,
-                                        void* stream) {
+                                        bool nhd, void* stream) {
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || max_kv_len <= 0)
         return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads and max_kv_len must be positive");
@@ -567,15 +595,16 @@ static pd_status contiguous_decode_impl(const void* q, const void* k_new, const 
     a.npv = npv;
     a.k_new = k_new;
     a.v_new = v_new;
-    return launch_decode(pl, a, head_dim, dtype, batch, static_cast<cudaStream_t>(stream));
+    return launch_decode(pl, a, head_dim, dtype, batch, nhd, static_cast<cudaStream_t>(stream));
 }
 
-pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int batch,
-                               int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len, int valid_kv_len,
-                               float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+pd_status pd_contiguous_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                               int batch, int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                               int valid_kv_len, float sm_scale, pd_dtype dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
     return contiguous_decode_impl(q, nullptr, nullptr, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
                                   head_dim, max_kv_len, valid_kv_len, sm_scale, dtype, workspace, workspace_bytes,
-                                  stream);
+                                  false, stream);
 }
 
 pd_status pd_contiguous_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -588,8 +617,31 @@ pd_status pd_contiguous_append_decode(const void* q, const void* k_new, const vo
         return fail(PD_ERR_INVALID, "position (%d) must be in [0, max_kv_len=%d)", position, max_kv_len);
     return contiguous_decode_impl(q, k_new, v_new, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
                                   head_dim, max_kv_len, position + 1, sm_scale, dtype, workspace, workspace_bytes,
-                                  stream);
+                                  false, stream);
 }
+
+pd_status pd_contiguous_decode_nhd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                               int batch, int num_qo_heads, int num_kv_heads, int head_dim, int max_kv_len,
+                               int valid_kv_len, float sm_scale, pd_dtype dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return contiguous_decode_impl(q, nullptr, nullptr, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
+                                  head_dim, max_kv_len, valid_kv_len, sm_scale, dtype, workspace, workspace_bytes,
+                                  true, stream);
+}
+
+pd_status pd_contiguous_append_decode_nhd(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                      void* v_cache, void* o, float* lse, int batch, int num_qo_heads,
+                                      int num_kv_heads, int head_dim, int max_kv_len, int position, float sm_scale,
+                                      pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_new || !v_new) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(PD_ERR_UNSUPPORTED, "k_new and v_new must be 16-byte aligned");
+    if (position < 0 || position >= max_kv_len)
+        return fail(PD_ERR_INVALID, "position (%d) must be in [0, max_kv_len=%d)", position, max_kv_len);
+    return contiguous_decode_impl(q, k_new, v_new, k_cache, v_cache, o, lse, batch, num_qo_heads, num_kv_heads,
+                                  head_dim, max_kv_len, position + 1, sm_scale, dtype, workspace, workspace_bytes,
+                                  true, stream);
+}
+
 
 pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, void* v_data, const int32_t* indices,
                           const int32_t* indptr, const int32_t* last_page_len, int batch, int num_kv_heads,
@@ -621,9 +673,9 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
     return ok();
 }
 
-pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
-                               int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
-                               void* stream) {
+static pd_status contiguous_append_impl(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                        int batch, int num_kv_heads, int head_dim, int max_kv_len, int position,
+                                        pd_dtype dtype, bool nhd, void* stream) {
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_kv_heads <= 0 || max_kv_len <= 0)
         return fail(PD_ERR_INVALID, "batch, num_kv_heads and max_kv_len must be positive");
@@ -642,11 +694,25 @@ pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cac
     const long long warps = (long long)batch * num_kv_heads;
     contiguous_append_kernel<<<unsigned((warps + 3) / 4), 128, 0, s>>>(
         static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), static_cast<uint8_t*>(k_cache),
-        static_cast<uint8_t*>(v_cache), batch, num_kv_heads, int(head_dim * elem_size(dtype)), max_kv_len, position);
+        static_cast<uint8_t*>(v_cache), batch, num_kv_heads, int(head_dim * elem_size(dtype)), max_kv_len, position, nhd ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (prof) mark(&g_prof.append_marks, s);
     if (e != cudaSuccess) return cuda_fail(e, "contiguous append launch");
     return ok();
+}
+
+pd_status pd_contiguous_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
+                               int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
+                               void* stream) {
+    return contiguous_append_impl(k_new, v_new, k_cache, v_cache, batch, num_kv_heads, head_dim, max_kv_len, position,
+                                  dtype, false, stream);
+}
+
+pd_status pd_contiguous_append_nhd(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int batch,
+                                   int num_kv_heads, int head_dim, int max_kv_len, int position, pd_dtype dtype,
+                                   void* stream) {
+    return contiguous_append_impl(k_new, v_new, k_cache, v_cache, batch, num_kv_heads, head_dim, max_kv_len, position,
+                                  dtype, true, stream);
 }
 
 pd_status pd_merge_states(const float* o_parts, const float* lse_parts, int num_parts, int num_rows, int head_dim,

@@ -63,9 +63,11 @@ struct Cfg {
     static_assert(kRC >= kRW && kRC % (kRW * kRR) == 0, "rows per stage");
 };
 
-// kFused: also perform the fused append (a.k_new / a.v_new set).
-template <typename T, int D, int G, bool kFused>
+// kVariant: kVarFused adds the fused append (a.k_new / a.v_new set); kVarNhd
+// reads a token-major contiguous cache, one bulk copy per row.
+template <typename T, int D, int G, int kVariant>
 __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
+    constexpr bool kFused = (kVariant & kVarFused) != 0, kNhd = (kVariant & kVarNhd) != 0;
     using C = Cfg<T, D, G>;
     using E = Elt<T>;
     constexpr int kL = C::kL, kRW = C::kRW, kRR = C::kRR, kV = C::kV, kVF = C::kVF;
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
             for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
         }
-        walk.prefetch_first_slabs(first_page, kStages, size_t(C::kRowBytes));
+        walk.template prefetch_first_slabs<kNhd>(first_page, kStages, size_t(C::kRowBytes));
     });
     __syncthreads();  // the only block-wide barrier: warps are independent from here on
     // Let the merge kernel be scheduled now; it waits for this grid before it
@@ -114,39 +116,52 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(C::kRowBytes);
-    // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
+    // Emit the next chunk into `slot` (whole warp). Lane 0 posts the byte
+    // count and issues the copies; in NHD order each lane r then copies row r.
     auto produce = [&](int slot) {
         Chunk ck;
         const bool have = walk.template next<kRC>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
         if constexpr (kFused) {
-            if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+            if (have && (ck.flags & kAppendRow)) write_new_row<kNhd>(a, ck, lane, row_bytes);
         }
-        if (lane != 0) return;
-        if (!have) {
-            meta[slot] = make_int4(0, kEndOfWork, 0, 0);
-            mbar_arrive(bar);
-            return;
+        const uint32_t kv_bytes = have ? uint32_t(ck.rows) * uint32_t(row_bytes) : 0u;
+        if (lane == 0) {
+            if (!have) {
+                meta[slot] = make_int4(0, kEndOfWork, 0, 0);
+                mbar_arrive(bar);
+            } else {
+                meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
+                const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
+                const uint32_t total = 2 * kv_bytes + q_bytes;
+                if (total == 0) {
+                    mbar_arrive(bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, total);
+                    if (!kNhd && kv_bytes) {
+                        const size_t off = kv_row<false>(a, ck.slab, ck.kh, ck.row0) * row_bytes;
+                        bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
+                        bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar,
+                                 policy);
+                    }
+                    if (q_bytes)
+                        bulk_g2s(smem_u32(st + 2 * kChunkBytes),
+                                 static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes, q_bytes, bar);
+                }
+            }
         }
-        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
-        const uint32_t kv_bytes = uint32_t(ck.rows) * uint32_t(row_bytes);
-        const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
-        const uint32_t total = 2 * kv_bytes + q_bytes;
-        if (total == 0) {
-            mbar_arrive(bar);
-            return;
+        if constexpr (kNhd) {
+            // after lane 0's expect_tx, so the barrier's phase cannot complete early
+            __syncwarp();
+            if (kv_bytes && lane < ck.rows) {
+                const size_t off = kv_row<true>(a, ck.slab, ck.kh, ck.row0 + lane) * row_bytes;
+                const uint32_t so = uint32_t(lane) * uint32_t(row_bytes);
+                bulk_g2s(smem_u32(st) + so, static_cast<const uint8_t*>(a.k) + off, uint32_t(row_bytes), bar, policy);
+                bulk_g2s(smem_u32(st + kChunkBytes) + so, static_cast<const uint8_t*>(a.v) + off, uint32_t(row_bytes),
+                         bar, policy);
+            }
         }
-        mbar_arrive_expect_tx(bar, total);
-        if (kv_bytes) {
-            const size_t off =
-                ((size_t(ck.slab) * a.num_kv_heads + ck.kh) * size_t(a.slab_rows) + size_t(ck.row0)) * row_bytes;
-            bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
-            bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar, policy);
-        }
-        if (q_bytes)
-            bulk_g2s(smem_u32(st + 2 * kChunkBytes), static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes,
-                     q_bytes, bar);
     };
 
     // ---- consumer state

@@ -63,10 +63,13 @@ __device__ __forceinline__ float2 unpack_pair(uint32_t w) {
     }
 }
 
-// kFused: also perform the fused append (a.k_new / a.v_new set).
-template <typename T, int D, bool kFused>
+// kVariant: kVarFused adds the fused append (a.k_new / a.v_new set); kVarNhd
+// reads a token-major contiguous cache, whose tensor maps are
+// {head_dim, kv heads, rows, slabs} (coordinates kv head and row swap).
+template <typename T, int D, int kVariant>
 __global__ void __launch_bounds__(256, 1)
     decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    constexpr bool kFused = (kVariant & kVarFused) != 0, kNhd = (kVariant & kVarNhd) != 0;
     using C = CfgMma<T, D>;
     constexpr int kS = C::kStages, kKS = C::kKSteps;
     // f16 P would lose small weights to underflow: weights are kept 2^7
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
         }
-        walk.prefetch_first_slabs(first_page, kS, size_t(D) * sizeof(T));
+        walk.template prefetch_first_slabs<kNhd>(first_page, kS, size_t(D) * sizeof(T));
     });
     __syncthreads();  // the only block-wide barrier
     launch_dependents();
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
         if constexpr (kFused) {
-            if (have && (ck.flags & kAppendRow)) write_new_row(a, ck, lane, row_bytes);
+            if (have && (ck.flags & kAppendRow)) write_new_row<kNhd>(a, ck, lane, row_bytes);
         }
         if (lane != 0) return;
         if (!have) {
@@ -138,11 +141,11 @@ __global__ void __launch_bounds__(256, 1)
         }
         mbar_arrive_expect_tx(bar, total);
         if (kv_bytes) {
+            const int c1 = kNhd ? ck.kh : ck.row0, c2 = kNhd ? ck.row0 : ck.kh;
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
-                tma_load_4d(st + bx * C::kBoxBytes, &tmk, bx * 64, ck.row0, ck.kh, ck.slab, bar, policy);
-                tma_load_4d(st + C::kKBytes + bx * C::kBoxBytes, &tmv, bx * 64, ck.row0, ck.kh, ck.slab, bar,
-                            policy);
+                tma_load_4d(st + bx * C::kBoxBytes, &tmk, bx * 64, c1, c2, ck.slab, bar, policy);
+                tma_load_4d(st + C::kKBytes + bx * C::kBoxBytes, &tmv, bx * 64, c1, c2, ck.slab, bar, policy);
             }
         }
         if (q_bytes)

@@ -12,7 +12,7 @@ namespace pd {
 // Kernels and sizes for one (T, head_dim, heads per tile) combination.
 struct KernelSet {
     const void* decode;
-    const void* decode_fused;  // the same decode with the fused append
+    const void* variant[4];  // decode kernel per variant bits (variant[0] == decode)
     const void* merge;
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
@@ -29,13 +29,13 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
         ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>);        \
         ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>);   \
         if constexpr (kHalf && GG == 8) {                                               \
-            ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, false>); \
+            ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, 0>);     \
             ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                 \
             ks->rows_per_stage = kMmaRows;                                              \
             ks->tensor_maps = 1;                                                        \
             ks->smem_slack = 1024;                                                      \
         } else {                                                                        \
-            ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, false>); \
+            ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);     \
             ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
             ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                   \
             ks->tensor_maps = 0;                                                        \
@@ -50,20 +50,20 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
     return false;
 }
 
-// The fused append + decode kernel for (T, head_dim, heads per tile); its
-// shared-memory layout is that of the plain decode kernel of lookup_kernels_t.
-// Instantiated in translation units of its own, so that the plain kernels
-// build in parallel with these.
-template <typename T>
-bool lookup_fused_t(int D, int G, const void** fn) {
+// The decode kernel of one variant (kVarFused / kVarNhd bits, not 0) for
+// (T, head_dim, heads per tile); its shared-memory layout is that of the plain
+// kernel of lookup_kernels_t. Each variant is instantiated in a translation
+// unit of its own, so that the variants build in parallel.
+template <typename T, int kVariant>
+bool lookup_variant_t(int D, int G, const void** fn) {
     constexpr bool kHalf = sizeof(T) == 2;
-#define PD_CASE(DD, GG)                                                             \
-    if (D == DD && G == GG) {                                                       \
-        if constexpr (kHalf && GG == 8)                                             \
-            *fn = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, true>);    \
-        else                                                                        \
-            *fn = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, true>);    \
-        return true;                                                                \
+#define PD_CASE(DD, GG)                                                                 \
+    if (D == DD && G == GG) {                                                           \
+        if constexpr (kHalf && GG == 8)                                                 \
+            *fn = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>);    \
+        else                                                                            \
+            *fn = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>);    \
+        return true;                                                                    \
     }
     PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)
     PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)

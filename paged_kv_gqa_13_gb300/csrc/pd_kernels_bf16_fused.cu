@@ -2,5 +2,7 @@
 #include "pd_kernels.cuh"
 
 namespace pd {
-bool lookup_fused_bf16(int head_dim, int heads, const void** fn) { return lookup_fused_t<__nv_bfloat16>(head_dim, heads, fn); }
+bool lookup_fused_bf16(int head_dim, int heads, const void** fn) {
+    return lookup_variant_t<__nv_bfloat16, 1>(head_dim, heads, fn);
+}
 }  // namespace pd

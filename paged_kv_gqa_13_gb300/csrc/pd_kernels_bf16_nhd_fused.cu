@@ -1,0 +1,8 @@
+// NHD contiguous fused append + decode kernels for element type __nv_bfloat16.
+#include "pd_kernels.cuh"
+
+namespace pd {
+bool lookup_nhd_fused_bf16(int head_dim, int heads, const void** fn) {
+    return lookup_variant_t<__nv_bfloat16, 3>(head_dim, heads, fn);
+}
+}  // namespace pd

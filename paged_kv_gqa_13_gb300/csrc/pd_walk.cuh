@@ -43,6 +43,21 @@ struct Chunk {
     int seg;    // segment id: pass * batch + b
 };
 
+// Variant bits of the decode kernels (compile-time, one instantiation each).
+constexpr int kVarFused = 1;  // the fused append (DecodeArgs::k_new set)
+constexpr int kVarNhd = 2;    // contiguous cache in NHD order [batch, max_kv_len, Hk, D]
+
+// Index, in head_dim-element rows, of row `row` of kv head kh in slab `slab`:
+// HND [slab, kv head, row] (pages and the HND contiguous cache) or NHD
+// [slab, row, kv head] (the token-major contiguous cache).
+template <bool kNhd>
+__device__ __forceinline__ size_t kv_row(const DecodeArgs& a, int slab, int kh, long long row) {
+    if constexpr (kNhd)
+        return (size_t(slab) * size_t(a.slab_rows) + size_t(row)) * size_t(a.num_kv_heads) + size_t(kh);
+    else
+        return (size_t(slab) * size_t(a.num_kv_heads) + size_t(kh)) * size_t(a.slab_rows) + size_t(row);
+}
+
 // kFused: the decode carries the fused append (DecodeArgs::k_new is set);
 // only then are new-row chunks marked.
 template <bool kFused>
@@ -163,6 +178,9 @@ struct Walk {
     // L2 as soon as their page ids are known, before the page table needed to
     // describe them has been staged. Whole slabs: pages hold page_size rows;
     // contiguous slabs are clipped to the cache.
+    // In NHD order the rows of one kv head are Hk rows apart: the span from
+    // the first to the last is prefetched (other heads' rows included).
+    template <bool kNhd>
     __device__ __forceinline__ void prefetch_first_slabs(int pg, int count, size_t row_bytes) {
         const long long p = p0 + lane;
         if (lane >= count || p >= pend) return;
@@ -174,13 +192,14 @@ struct Walk {
             const int b = i / a.npv;
             const long long r0 = (long long)(i % a.npv) * a.vpage;
             rows = min((long long)a.vpage, a.slab_rows - r0);
-            row = (size_t(b) * a.num_kv_heads + kh) * size_t(a.slab_rows) + size_t(r0);
+            row = kv_row<kNhd>(a, b, kh, r0);
         } else {
             if (pg < 0 || pg >= a.num_total_pages) return;
             rows = a.page_size;
-            row = (size_t(pg) * a.num_kv_heads + kh) * size_t(a.slab_rows);
+            row = kv_row<false>(a, pg, kh, 0);
         }
         if (rows <= 0) return;
+        if constexpr (kNhd) rows = (rows - 1) * a.num_kv_heads + 1;
         const uint32_t bytes = uint32_t(rows * (long long)row_bytes);
         bulk_prefetch_l2(static_cast<const uint8_t*>(a.k) + row * row_bytes, bytes);
         bulk_prefetch_l2(static_cast<const uint8_t*>(a.v) + row * row_bytes, bytes);
@@ -261,11 +280,11 @@ struct Walk {
 // slab), then fences them so that the chunk's copy, issued afterwards by
 // lane 0, reads them. Every warp whose chunk holds the row writes it (the same
 // bytes), so no warp depends on another's store.
+template <bool kNhd>
 __device__ __forceinline__ void write_new_row(const DecodeArgs& a, const Chunk& ck, int lane, size_t row_bytes) {
     const int b = ck.seg % a.batch;
     const size_t src = (size_t(b) * a.num_kv_heads + ck.kh) * row_bytes;
-    const size_t dst =
-        ((size_t(ck.slab) * a.num_kv_heads + ck.kh) * size_t(a.slab_rows) + size_t(ck.row0 + ck.rows - 1)) * row_bytes;
+    const size_t dst = kv_row<kNhd>(a, ck.slab, ck.kh, ck.row0 + ck.rows - 1) * row_bytes;
     uint8_t* kd = static_cast<uint8_t*>(const_cast<void*>(a.k)) + dst;
     uint8_t* vd = static_cast<uint8_t*>(const_cast<void*>(a.v)) + dst;
     const uint8_t* ks = static_cast<const uint8_t*>(a.k_new) + src;
