@@ -137,6 +137,8 @@ def load_workload(name: str, rank: int = 0):
 
     if name == "long_context_contiguous":
         return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous"
+    if name == "long_context_nhd":
+        return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous_nhd"
     return wl.CONFIGS[name](seed=wl.CONFIGS[name].__defaults__[0] + 100 * rank), "paged"
 
 
@@ -182,16 +184,20 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     lse = torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device=dev)
     tables = [w.table]
     appends = []
-    if mode == "contiguous":
+    if mode.startswith("contiguous"):
         kc, vc, n_valid = wl.contiguous_copy(w)
         k = to_dev(kc, w.dtype, dev)
         v = to_dev(vc, w.dtype, dev)
         del kc, vc
+        decode = pd.pd_contiguous_decode
+        if mode == "contiguous_nhd":  # token-major [batch, max_kv_len, Hk, D]
+            k, v = k.transpose(1, 2).contiguous(), v.transpose(1, 2).contiguous()
+            decode = pd.pd_contiguous_decode_nhd
         ws = pd.alloc_workspace(pd.pd_contiguous_decode_workspace_bytes(
             w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, code), dev)
 
         def step(i):
-            pd.pd_contiguous_decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
+            decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
         bytes_per_step = [algorithmic_bytes(w)]
         decode_bytes_per_step = bytes_per_step
     else:
@@ -386,12 +392,15 @@ def cpu_baseline(w, mode: str, budget_s: float = 12.0) -> dict:
     table = w.table
     if w.append_steps:
         table = wl.table_after_append(w.table)
-    if mode == "contiguous":
+    layout = "nhd" if mode == "contiguous_nhd" else "hnd"
+    if mode.startswith("contiguous"):
         kc, vc, nv = wl.contiguous_copy(w)
+        if layout == "nhd":
+            kc, vc = np.ascontiguousarray(kc.transpose(0, 2, 1, 3)), np.ascontiguousarray(vc.transpose(0, 2, 1, 3))
     n, t0 = 0, time.perf_counter()
     while True:
-        if mode == "contiguous":
-            oracle.contiguous_decode(w.q, kc, vc, w.num_qo_heads, nv, w.sm_scale, w.dtype, threads)
+        if mode.startswith("contiguous"):
+            oracle.contiguous_decode(w.q, kc, vc, w.num_qo_heads, nv, w.sm_scale, w.dtype, threads, layout=layout)
         else:
             oracle.paged_decode_workload(w, table=table, threads=threads)
         n += 1
@@ -410,8 +419,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG,
-                    choices=["tiny", "llama3_8b", "long_context", "long_context_contiguous", "ragged_70b",
-                             "mha_append"])
+                    choices=["tiny", "llama3_8b", "long_context", "long_context_contiguous", "long_context_nhd",
+                             "ragged_70b", "mha_append"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--append", default="fused", choices=["fused", "separate"],
                     help="append workloads: one fused append + decode launch, or an append launch then a decode")
@@ -459,7 +468,8 @@ def main():
     dec_bytes = r["decode_bytes_mean"]  # the decode kernel's own bytes (no append rows)
     achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
     kname = decode_kernel_name(w)
-    traffic = recorded_traffic(kname, w.name + ("/contiguous" if r["mode"] == "contiguous" else ""))
+    traffic = recorded_traffic(kname, w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd"}
+                                                .get(r["mode"], "")))
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
                 "peak_source": peaks["source"], "kernel": kname,

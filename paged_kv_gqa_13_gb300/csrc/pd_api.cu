@@ -228,30 +228,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K or V as a 4-D tensor of 16-bit elements, {head_dim, slab_rows, kv heads,
-// slabs} (HND) or {head_dim, kv heads, slab_rows, slabs} (NHD), read in boxes
-// of 64 columns x 16 rows of one kv head with the 128-byte swizzle; rows
-// outside the tensor read as zero. Either way a box lands as 16 rows of 128
-// bytes.
-pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long slab_rows, int Hk,
-                      long long slabs, bool nhd) {
+// K or V as a 4-D tensor {head_dim, rows, kv heads, slabs} (HND) or
+// {head_dim, kv heads, rows, slabs} (NHD). `rows` is the extent read (page
+// size, or the valid length of a contiguous cache), `slab_rows` the rows
+// allocated per (slab, kv head) that set the strides; rows past `rows` read as
+// zero. mma: boxes of 64 columns x 16 rows with the 128-byte swizzle (the
+// tensor-core kernel). Otherwise: unswizzled boxes of head_dim columns x
+// `box_rows` rows (the CUDA-core kernel on an NHD cache). A box holds rows of
+// one kv head, so it lands as consecutive rows either way.
+pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long rows, long long slab_rows,
+                      int Hk, long long slabs, bool nhd, bool mma, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t row = cuuint64_t(D) * 2;
-    const cuuint64_t dims_hnd[4] = {cuuint64_t(D), cuuint64_t(slab_rows), cuuint64_t(Hk), cuuint64_t(slabs)};
-    const cuuint64_t dims_nhd[4] = {cuuint64_t(D), cuuint64_t(Hk), cuuint64_t(slab_rows), cuuint64_t(slabs)};
+    const cuuint64_t row = cuuint64_t(D) * elem_size(dt);
+    const cuuint64_t dims_hnd[4] = {cuuint64_t(D), cuuint64_t(rows), cuuint64_t(Hk), cuuint64_t(slabs)};
+    const cuuint64_t dims_nhd[4] = {cuuint64_t(D), cuuint64_t(Hk), cuuint64_t(rows), cuuint64_t(slabs)};
     const cuuint64_t str_hnd[3] = {row, cuuint64_t(slab_rows) * row, cuuint64_t(Hk) * slab_rows * row};
     const cuuint64_t str_nhd[3] = {row, cuuint64_t(Hk) * row, cuuint64_t(Hk) * slab_rows * row};
     const cuuint64_t* dims = nhd ? dims_nhd : dims_hnd;
     const cuuint64_t* strides = nhd ? str_nhd : str_hnd;
-    const cuuint32_t box_hnd[4] = {64, cuuint32_t(pd::kMmaRows), 1, 1};
-    const cuuint32_t box_nhd[4] = {64, 1, cuuint32_t(pd::kMmaRows), 1};
+    const cuuint32_t cols = mma ? 64u : cuuint32_t(D);
+    const cuuint32_t brows = mma ? cuuint32_t(pd::kMmaRows) : cuuint32_t(box_rows);
+    const cuuint32_t box_hnd[4] = {cols, brows, 1, 1};
+    const cuuint32_t box_nhd[4] = {cols, 1, brows, 1};
     const cuuint32_t* box = nhd ? box_nhd : box_hnd;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = enc(map, dt == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType ty = dt == PD_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == PD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUresult r = enc(map, ty, 4, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return PD_OK;
 }
@@ -293,10 +300,18 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, bool nhd,
                         cudaStream_t stream) {
     const int variant = (a.k_new != nullptr ? pd::kVarFused : 0) | (nhd ? pd::kVarNhd : 0);
+    // Every decode kernel takes two tensor maps; they are read by the
+    // tensor-core kernel and by the CUDA-core kernel's NHD variants.
     CUtensorMap maps[2];
-    if (pl.ks.tensor_maps && a.total_pos > 0) {
-        pd_status st = make_kv_map(&maps[0], a.k, dt, D, a.slab_rows, a.num_kv_heads, slabs, nhd);
-        if (st == PD_OK) st = make_kv_map(&maps[1], a.v, dt, D, a.slab_rows, a.num_kv_heads, slabs, nhd);
+    std::memset(maps, 0, sizeof(maps));
+    if ((pl.ks.mma || nhd) && a.total_pos > 0) {
+        const long long rows = a.contiguous ? a.valid_kv_len : a.slab_rows;
+        const bool mma = pl.ks.mma != 0;
+        pd_status st = make_kv_map(&maps[0], a.k, dt, D, rows, a.slab_rows, a.num_kv_heads, slabs, nhd, mma,
+                                   pl.ks.rows_per_stage);
+        if (st == PD_OK)
+            st = make_kv_map(&maps[1], a.v, dt, D, rows, a.slab_rows, a.num_kv_heads, slabs, nhd, mma,
+                             pl.ks.rows_per_stage);
         if (st != PD_OK) return st;
     }
     std::unique_lock<std::mutex> plk(g_prof_mu);

@@ -64,9 +64,13 @@ struct Cfg {
 };
 
 // kVariant: kVarFused adds the fused append (a.k_new / a.v_new set); kVarNhd
-// reads a token-major contiguous cache, one bulk copy per row.
+// reads a token-major contiguous cache through the tensor maps tmk / tmv
+// ({head_dim, kv heads, valid rows, requests}, boxes of kRC rows of one kv
+// head, unswizzled, rows past the valid length zero-filled); the other
+// variants do not read the maps.
 template <typename T, int D, int G, int kVariant>
-__global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(256, 1)
+    decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kFused = (kVariant & kVarFused) != 0, kNhd = (kVariant & kVarNhd) != 0;
     using C = Cfg<T, D, G>;
     using E = Elt<T>;
@@ -93,6 +97,12 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
+    if constexpr (kNhd) {
+        if (lane == 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+    }
 
     // ---- set-up: stage the page table, zero the ring, init the barriers
     walk.stage_table(s_indptr, s_lpl, [&] {
@@ -116,8 +126,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(C::kRowBytes);
-    // Emit the next chunk into `slot` (whole warp). Lane 0 posts the byte
-    // count and issues the copies; in NHD order each lane r then copies row r.
+    // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot) {
         Chunk ck;
         const bool have = walk.template next<kRC>(&ck);
@@ -126,42 +135,36 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const DecodeArgs a) {
         if constexpr (kFused) {
             if (have && (ck.flags & kAppendRow)) write_new_row<kNhd>(a, ck, lane, row_bytes);
         }
-        const uint32_t kv_bytes = have ? uint32_t(ck.rows) * uint32_t(row_bytes) : 0u;
-        if (lane == 0) {
-            if (!have) {
-                meta[slot] = make_int4(0, kEndOfWork, 0, 0);
-                mbar_arrive(bar);
+        if (lane != 0) return;
+        if (!have) {
+            meta[slot] = make_int4(0, kEndOfWork, 0, 0);
+            mbar_arrive(bar);
+            return;
+        }
+        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
+        // An NHD box lands whole: kRC rows, those past the valid length as zeros.
+        const uint32_t kv_bytes =
+            kNhd ? (ck.rows > 0 ? uint32_t(kChunkBytes) : 0u) : uint32_t(ck.rows) * uint32_t(row_bytes);
+        const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
+        const uint32_t total = 2 * kv_bytes + q_bytes;
+        if (total == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, total);
+        if (kv_bytes) {
+            if constexpr (kNhd) {
+                tma_load_4d(smem_u32(st), &tmk, 0, ck.kh, ck.row0, ck.slab, bar, policy);
+                tma_load_4d(smem_u32(st + kChunkBytes), &tmv, 0, ck.kh, ck.row0, ck.slab, bar, policy);
             } else {
-                meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
-                const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
-                const uint32_t total = 2 * kv_bytes + q_bytes;
-                if (total == 0) {
-                    mbar_arrive(bar);
-                } else {
-                    mbar_arrive_expect_tx(bar, total);
-                    if (!kNhd && kv_bytes) {
-                        const size_t off = kv_row<false>(a, ck.slab, ck.kh, ck.row0) * row_bytes;
-                        bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
-                        bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar,
-                                 policy);
-                    }
-                    if (q_bytes)
-                        bulk_g2s(smem_u32(st + 2 * kChunkBytes),
-                                 static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes, q_bytes, bar);
-                }
+                const size_t off = kv_row<false>(a, ck.slab, ck.kh, ck.row0) * row_bytes;
+                bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
+                bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar, policy);
             }
         }
-        if constexpr (kNhd) {
-            // after lane 0's expect_tx, so the barrier's phase cannot complete early
-            __syncwarp();
-            if (kv_bytes && lane < ck.rows) {
-                const size_t off = kv_row<true>(a, ck.slab, ck.kh, ck.row0 + lane) * row_bytes;
-                const uint32_t so = uint32_t(lane) * uint32_t(row_bytes);
-                bulk_g2s(smem_u32(st) + so, static_cast<const uint8_t*>(a.k) + off, uint32_t(row_bytes), bar, policy);
-                bulk_g2s(smem_u32(st + kChunkBytes) + so, static_cast<const uint8_t*>(a.v) + off, uint32_t(row_bytes),
-                         bar, policy);
-            }
-        }
+        if (q_bytes)
+            bulk_g2s(smem_u32(st + 2 * kChunkBytes), static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes,
+                     q_bytes, bar);
     };
 
     // ---- consumer state

@@ -3,6 +3,7 @@
 // conversions, warp reductions and the kernel argument blocks.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

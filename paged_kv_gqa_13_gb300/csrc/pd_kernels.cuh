@@ -17,7 +17,7 @@ struct KernelSet {
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
     int rows_per_stage;  // K (and V) rows one pipeline stage holds
-    int tensor_maps;     // 1: the decode kernel takes K and V tensor maps (tensor-core kernel)
+    int mma;             // 1: tensor-core kernel (K/V always through 128B-swizzled tensor maps)
     int smem_slack;      // extra dynamic shared memory for aligning the stages
 };
 
@@ -32,13 +32,13 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
             ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, 0>);     \
             ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                 \
             ks->rows_per_stage = kMmaRows;                                              \
-            ks->tensor_maps = 1;                                                        \
+            ks->mma = 1;                                                                \
             ks->smem_slack = 1024;                                                      \
         } else {                                                                        \
             ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);     \
             ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
             ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                   \
-            ks->tensor_maps = 0;                                                        \
+            ks->mma = 0;                                                                \
             ks->smem_slack = 0;                                                         \
         }                                                                               \
         return true;                                                                    \
