@@ -57,9 +57,15 @@ def _lib():
         lib.oracle_merge_states.argtypes = [_P, _P, _I, _L, _I, _P, _P]
         lib.oracle_contiguous_append.argtypes = [_P, _P, _P, _P, _I, _I, _I, _L, _L, _I, _I]
         lib.oracle_round_to_dtype.argtypes = [_P, _L, _I, _P]
+        lib.oracle_paged_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _L,
+                                                ctypes.c_float, _I, _P, _P, _I]
+        lib.oracle_paged_append_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]
+        lib.oracle_e4m3_values.argtypes = [_P, _L, _P]
+        lib.oracle_e4m3_round.argtypes = [_P, _L, _P]
         for f in (lib.oracle_decode_elements, lib.oracle_paged_decode, lib.oracle_contiguous_decode,
                   lib.oracle_paged_append, lib.oracle_merge_states, lib.oracle_round_to_dtype,
-                  lib.oracle_contiguous_append):
+                  lib.oracle_contiguous_append, lib.oracle_paged_decode_fp8, lib.oracle_paged_append_fp8,
+                  lib.oracle_e4m3_values, lib.oracle_e4m3_round):
             f.restype = _I
         lib.oracle_hardware_threads.restype = _I
         _handle = lib
@@ -107,6 +113,62 @@ def paged_decode(q, k_data, v_data, indices, indptr, last_page_len, num_qo_heads
     if rc:
         raise OracleError(f"oracle_paged_decode returned {rc}")
     return o, lse
+
+
+def e4m3_values(codes) -> np.ndarray:
+    """Exact float64 values of E4M3 codes (uint8 array); NaN for the NaN codes."""
+    codes = _c(np.asarray(codes), np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _lib().oracle_e4m3_values(codes.ctypes.data, codes.size, out.ctypes.data)
+    return out
+
+
+def e4m3_round(x) -> np.ndarray:
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at +-448."""
+    x = _c(np.asarray(x), np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _lib().oracle_e4m3_round(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def paged_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, indices, indptr, last_page_len, num_qo_heads,
+                     num_kv_heads, head_dim, page_size, sm_scale, q_dtype, threads: int = 0):
+    """Decode over an FP8 pool (E4M3 codes, value = code value * scale[kv head]); float64 o, lse."""
+    q, k_codes, v_codes = _c(q), _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    k_scale, v_scale = _c(np.asarray(k_scale), np.float32), _c(np.asarray(v_scale), np.float32)
+    indices = _c(np.asarray(indices), np.int32)
+    indptr = _c(np.asarray(indptr), np.int32)
+    last_page_len = _c(np.asarray(last_page_len), np.int32)
+    batch = len(indptr) - 1
+    o = np.empty((batch, num_qo_heads, head_dim), dtype=np.float64)
+    lse = np.empty((batch, num_qo_heads), dtype=np.float64)
+    rc = _lib().oracle_paged_decode_fp8(q.ctypes.data, k_codes.ctypes.data, v_codes.ctypes.data,
+                                        k_scale.ctypes.data, v_scale.ctypes.data,
+                                        indices.ctypes.data if indices.size else None, indptr.ctypes.data,
+                                        last_page_len.ctypes.data, batch, num_qo_heads, num_kv_heads, head_dim,
+                                        page_size, k_codes.shape[0], indices.size, float(sm_scale),
+                                        DTYPE_CODE[q_dtype], o.ctypes.data, lse.ctypes.data, threads)
+    if rc:
+        raise OracleError(f"oracle_paged_decode_fp8 returned {rc}")
+    return o, lse
+
+
+def paged_append_fp8(k_new, v_new, k_scale, v_scale, k_codes, v_codes, indices, indptr, last_page_len, dtype):
+    """Quantise the new rows into the host mirrors k_codes / v_codes (uint8 pools) in place."""
+    k_new, v_new = _c(k_new), _c(v_new)
+    k_scale, v_scale = _c(np.asarray(k_scale), np.float32), _c(np.asarray(v_scale), np.float32)
+    assert k_codes.flags.c_contiguous and v_codes.flags.c_contiguous
+    indices = _c(np.asarray(indices), np.int32)
+    indptr = _c(np.asarray(indptr), np.int32)
+    last_page_len = _c(np.asarray(last_page_len), np.int32)
+    num_total_pages, num_kv_heads, page_size, head_dim = k_codes.shape
+    rc = _lib().oracle_paged_append_fp8(k_new.ctypes.data, v_new.ctypes.data, k_scale.ctypes.data,
+                                        v_scale.ctypes.data, k_codes.ctypes.data, v_codes.ctypes.data,
+                                        indices.ctypes.data, indptr.ctypes.data, last_page_len.ctypes.data,
+                                        len(indptr) - 1, num_kv_heads, head_dim, page_size, num_total_pages,
+                                        DTYPE_CODE[dtype])
+    if rc:
+        raise OracleError(f"oracle_paged_append_fp8 returned {rc}")
 
 
 def paged_decode_workload(w, table=None, threads: int = 0):

@@ -92,6 +92,36 @@ struct View {
 
 size_t elem_bytes(int dtype) { return dtype == DT_F32 ? 4 : 2; }
 
+// FP8 E4M3 as the OCP 8-bit floating point specification (OFP8) defines it:
+// sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
+// the subnormals (m / 8) * 2^-6; S.1111.111 is NaN; there is no infinity, so
+// S.1111.110 = 448 is the largest finite magnitude.
+double e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+    const int bias = ORACLE_MUTANT == 12 ? 8 : 7;
+    const double v = e == 0 ? std::ldexp(m / 8.0, 1 - bias) : std::ldexp(1.0 + m / 8.0, e - bias);
+    return s ? -v : v;
+}
+
+// Round to E4M3, nearest with ties to the even code, finite values past 448
+// (and infinities) saturating to +-448, NaN to the NaN code 0x7F. By brute
+// force over the 127 non-negative finite codes (their values increase with
+// the code, and of two neighbours exactly one has an even code).
+uint8_t e4m3_round(float x) {
+    if (std::isnan(x)) return 0x7F;
+    const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+    const double a = std::fabs(double(x));
+    if (std::isinf(a)) return sign | 0x7E;
+    int best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double err = std::fabs(e4m3_value(uint8_t(c)) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) best = c, best_err = err;
+    }
+    return uint8_t(sign | best);
+}
+
 template <class F>
 void parallel_for(long n, int nthreads, F f) {
     if (nthreads <= 0) nthreads = int(std::thread::hardware_concurrency());
@@ -141,6 +171,48 @@ void attend(const View& q, size_t q_off, long n, int D, double scale, KAt k_at, 
 
 }  // namespace
 
+// Shared by the paged decodes: validates the table ([P3] "Layout") and runs
+// attend() for every (request, q head), with kval(i, kh) / vval(i, kh) the
+// value of element i of the K / V pool, which belongs to kv head kh.
+template <class KV, class VV>
+int paged_decode_values(const void* q, int q_dtype, KV kval, VV vval, const int32_t* indices,
+                        const int32_t* indptr, const int32_t* last_page_len, int batch, int num_qo_heads,
+                        int num_kv_heads, int head_dim, int page_size, int num_total_pages, long num_indices,
+                        float sm_scale, double* o_out, double* lse_out, int nthreads) {
+    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+        num_total_pages <= 0 || q_dtype < 0 || q_dtype > 2)
+        return 1;
+    if (num_qo_heads % num_kv_heads != 0) return 1;  // [P3] "Constraints": integer group
+    if (indptr[0] < 0) return 2;
+    for (int b = 0; b < batch; ++b) {
+        if (indptr[b + 1] < indptr[b]) return 2;
+        if (indptr[b + 1] > indptr[b] && (last_page_len[b] < 0 || last_page_len[b] > page_size)) return 2;
+    }
+    if (indptr[batch] > num_indices) return 2;
+    for (long i = indptr[0]; i < indptr[batch]; ++i)
+        if (indices[i] < 0 || indices[i] >= num_total_pages) return 2;
+
+    const int group = num_qo_heads / num_kv_heads;
+    const View Q{q, q_dtype};
+    const double scale = double(sm_scale);
+    parallel_for(long(batch) * num_qo_heads, nthreads, [&](long bh) {
+        const int b = int(bh / num_qo_heads), h = int(bh % num_qo_heads);
+        const int kh = ORACLE_MUTANT == 5 ? h % num_kv_heads : h / group;  // [P2] gqa_decode: kv_h = h / group_size
+        const long np = indptr[b + 1] - indptr[b];
+        const long n = np == 0 ? 0 : (np - 1) * page_size + (ORACLE_MUTANT == 6 ? page_size : last_page_len[b]);
+        auto addr = [&](long t, int d) {
+            const size_t page = size_t(indices[indptr[b] + t / page_size]);
+            const size_t row = size_t(ORACLE_MUTANT == 7 ? page_size - 1 - t % page_size : t % page_size);
+            return ((page * num_kv_heads + kh) * page_size + row) * head_dim + size_t(d);
+        };
+        attend(Q, size_t(bh) * head_dim, n, head_dim, scale,
+               [&](long t, int d) { return kval(addr(t, d), kh); },
+               [&](long t, int d) { return vval(addr(t, d), kh); },
+               o_out + size_t(bh) * head_dim, lse_out + bh);
+    });
+    return 0;
+}
+
 extern "C" {
 
 // Decode nelem elements of a raw array of dtype into doubles.
@@ -163,37 +235,41 @@ int oracle_paged_decode(const void* q, const void* k_data, const void* v_data,
                         int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                         int num_total_pages, long num_indices, float sm_scale, int dtype,
                         double* o_out, double* lse_out, int nthreads) {
-    if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
-        num_total_pages <= 0 || dtype < 0 || dtype > 2)
-        return 1;
-    if (num_qo_heads % num_kv_heads != 0) return 1;  // [P3] "Constraints": integer group
-    if (indptr[0] < 0) return 2;
-    for (int b = 0; b < batch; ++b) {
-        if (indptr[b + 1] < indptr[b]) return 2;
-        if (indptr[b + 1] > indptr[b] && (last_page_len[b] < 0 || last_page_len[b] > page_size)) return 2;
-    }
-    if (indptr[batch] > num_indices) return 2;
-    for (long i = indptr[0]; i < indptr[batch]; ++i)
-        if (indices[i] < 0 || indices[i] >= num_total_pages) return 2;
+    if (dtype < 0 || dtype > 2) return 1;
+    const View K{k_data, dtype}, V{v_data, dtype};
+    return paged_decode_values(
+        q, dtype, [&](size_t i, int) { return K.at(i); }, [&](size_t i, int) { return V.at(i); }, indices, indptr,
+        last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices,
+        sm_scale, o_out, lse_out, nthreads);
+}
 
-    const int group = num_qo_heads / num_kv_heads;
-    const View Q{q, dtype}, K{k_data, dtype}, V{v_data, dtype};
-    const double scale = double(sm_scale);
-    parallel_for(long(batch) * num_qo_heads, nthreads, [&](long bh) {
-        const int b = int(bh / num_qo_heads), h = int(bh % num_qo_heads);
-        const int kh = ORACLE_MUTANT == 5 ? h % num_kv_heads : h / group;  // [P2] gqa_decode: kv_h = h / group_size
-        const long np = indptr[b + 1] - indptr[b];
-        const long n = np == 0 ? 0 : (np - 1) * page_size + (ORACLE_MUTANT == 6 ? page_size : last_page_len[b]);
-        auto addr = [&](long t, int d) {
-            const size_t page = size_t(indices[indptr[b] + t / page_size]);
-            const size_t row = size_t(ORACLE_MUTANT == 7 ? page_size - 1 - t % page_size : t % page_size);
-            return ((page * num_kv_heads + kh) * page_size + row) * head_dim + size_t(d);
-        };
-        attend(Q, size_t(bh) * head_dim, n, head_dim, scale,
-               [&](long t, int d) { return K.at(addr(t, d)); },
-               [&](long t, int d) { return V.at(addr(t, d)); },
-               o_out + size_t(bh) * head_dim, lse_out + bh);
-    });
+// The paged decode over an FP8 pool: K and V pages hold E4M3 codes (one byte
+// per element, same HND layout), and element value = e4m3_value(code) *
+// k_scale[kh] (v_scale[kh] for V), kh the element's kv head. q and o are
+// q_dtype (f16 or bf16). This is this library's own extension, not a layout
+// of the pages: a per-kv-head scale is the plainest scheme that keeps the
+// pool one byte per element.
+int oracle_paged_decode_fp8(const void* q, const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scale,
+                            const float* v_scale, const int32_t* indices, const int32_t* indptr,
+                            const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads,
+                            int head_dim, int page_size, int num_total_pages, long num_indices, float sm_scale,
+                            int q_dtype, double* o_out, double* lse_out, int nthreads) {
+    if (q_dtype != DT_F16 && q_dtype != DT_BF16) return 1;
+    const float* vs = ORACLE_MUTANT == 13 ? k_scale : v_scale;
+    return paged_decode_values(
+        q, q_dtype, [&](size_t i, int kh) { return e4m3_value(k_codes[i]) * double(k_scale[kh]); },
+        [&](size_t i, int kh) { return e4m3_value(v_codes[i]) * double(vs[kh]); }, indices, indptr,
+        last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices,
+        sm_scale, o_out, lse_out, nthreads);
+}
+
+// E4M3 codes of values / per-element conversions, for the pins.
+int oracle_e4m3_values(const uint8_t* codes, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+    return 0;
+}
+int oracle_e4m3_round(const float* x, long n, uint8_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_round(x[i]);
     return 0;
 }
 
@@ -264,6 +340,35 @@ int oracle_paged_append(const void* k_new, const void* v_new, void* k_data, void
             std::memcpy(static_cast<uint8_t*>(k_data) + dst, static_cast<const uint8_t*>(k_new) + src, row);
             std::memcpy(static_cast<uint8_t*>(v_data) + dst, static_cast<const uint8_t*>(v_new) + src, row);
         }
+    }
+    return 0;
+}
+
+// Paged append into an FP8 pool: the slot of oracle_paged_append receives
+// the codes e4m3_round(x / scale[h]) of the new row, x the exact value of the
+// f16 / bf16 element widened to f32 and the division done in f32 (the
+// quantisation decision is made in f32 on both sides of a parity test).
+// Returns 0, 1 for a bad descriptor, 2 for a bad table entry.
+int oracle_paged_append_fp8(const void* k_new, const void* v_new, const float* k_scale, const float* v_scale,
+                            uint8_t* k_codes, uint8_t* v_codes, const int32_t* indices, const int32_t* indptr,
+                            const int32_t* last_page_len, int batch, int num_kv_heads, int head_dim, int page_size,
+                            int num_total_pages, int new_dtype) {
+    if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_total_pages <= 0 ||
+        (new_dtype != DT_F16 && new_dtype != DT_BF16))
+        return 1;
+    const View KN{k_new, new_dtype}, VN{v_new, new_dtype};
+    for (int b = 0; b < batch; ++b) {
+        if (indptr[b + 1] <= indptr[b]) return 2;
+        const int slot = last_page_len[b] - 1;
+        const int page = indices[indptr[b + 1] - 1];
+        if (slot < 0 || slot >= page_size || page < 0 || page >= num_total_pages) return 2;
+        for (int h = 0; h < num_kv_heads; ++h)
+            for (int d = 0; d < head_dim; ++d) {
+                const size_t dst = ((size_t(page) * num_kv_heads + h) * page_size + size_t(slot)) * head_dim + d;
+                const size_t src = (size_t(b) * num_kv_heads + h) * head_dim + d;
+                k_codes[dst] = e4m3_round(float(KN.at(src)) / k_scale[h]);
+                v_codes[dst] = e4m3_round(float(VN.at(src)) / v_scale[h]);
+            }
     }
     return 0;
 }

@@ -443,3 +443,115 @@ def test_nhd_append_writes_token_position_of_every_head():
             fkb[off:off + D] = kn[b, h]
     assert np.array_equal(fk, fkb)  # nothing else changed
     assert np.array_equal(vc[:, n], vn) and np.array_equal(np.delete(vc, n, axis=1), np.delete(vb, n, axis=1))
+
+
+# --- FP8 E4M3 pools: value = code value * per-kv-head scale ---------------------------------
+# The code values follow the OCP 8-bit floating point specification (OFP8), E4M3:
+# bias 7, 3 mantissa bits, subnormals (m/8)*2^-6, S.1111.111 NaN, no infinity.
+
+def test_e4m3_values_at_the_format_anchors():
+    anchors = {0x00: 0.0, 0x01: 2.0**-9, 0x07: 7 * 2.0**-9, 0x08: 2.0**-6, 0x0F: 1.875 * 2.0**-6,
+               0x30: 0.5, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x78: 256.0, 0x7E: 448.0}
+    codes = np.array(list(anchors), dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_values(codes), np.array(list(anchors.values())))
+    assert np.array_equal(oracle.e4m3_values(codes | 0x80), -np.array(list(anchors.values())))
+    allv = oracle.e4m3_values(np.arange(256, dtype=np.uint8))
+    assert set(np.flatnonzero(np.isnan(allv))) == {0x7F, 0xFF}
+    pos = allv[:0x7F]
+    assert np.all(np.diff(pos) > 0)  # magnitudes increase with the code
+    assert np.signbit(allv[0x80]) and allv[0x80] == 0.0
+    fin = allv[~np.isnan(allv)]
+    assert np.array_equal(fin.astype(np.float16).astype(np.float64), fin)  # every value is an f16
+
+
+def test_e4m3_round_is_nearest_even_and_saturates():
+    codes = np.arange(0x7F, dtype=np.uint8)
+    vals = oracle.e4m3_values(codes)
+    assert np.array_equal(oracle.e4m3_round(vals.astype(np.float32)), codes)
+    assert np.array_equal(oracle.e4m3_round(-vals[1:].astype(np.float32)), codes[1:] | 0x80)
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)  # exact: one more mantissa bit
+    assert np.array_equal(mids.astype(np.float64), (vals[:-1] + vals[1:]) / 2)
+    even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[:-1] + 1)
+    assert np.array_equal(oracle.e4m3_round(mids), even)
+    assert np.array_equal(oracle.e4m3_round(np.nextafter(mids, np.float32(np.inf))), codes[1:])
+    assert np.array_equal(oracle.e4m3_round(np.nextafter(mids, np.float32(0))), codes[:-1])
+    big = np.array([448.0, 449.0, 464.0, 1e6, np.inf, -500.0, -np.inf], dtype=np.float32)
+    assert list(oracle.e4m3_round(big)) == [0x7E] * 5 + [0xFE] * 2
+    assert oracle.e4m3_round(np.array([np.nan], dtype=np.float32))[0] == 0x7F
+
+
+def _fp8_workload(seed, q_dtype="f16", pow2_scales=False, lens=(0, 1, 15, 16, 17, 200), Hq=8, Hk=2, D=64, P=16):
+    w = wl.make_paged(f"fp8_{seed}", q_dtype, list(lens), Hq, Hk, D, P, seed)
+    k8, v8, ks, vs = wl.fp8_pool(w)
+    if pow2_scales:
+        ks = np.array([2.0 ** -(2 + h % 3) for h in range(Hk)], dtype=np.float32)
+        vs = np.array([2.0 ** -(1 + h % 4) for h in range(Hk)], dtype=np.float32)
+    return w, k8, v8, ks, vs
+
+
+def _fp8_decode(w, k8, v8, ks, vs, q=None, sm_scale=None):
+    t = w.table
+    return oracle.paged_decode_fp8(w.q if q is None else q, k8, v8, ks, vs, t.indices, t.indptr, t.last_page_len,
+                                   w.num_qo_heads, w.num_kv_heads, w.head_dim, t.page_size,
+                                   w.sm_scale if sm_scale is None else sm_scale, w.dtype)
+
+
+def test_fp8_decode_equals_f32_decode_of_the_dequantised_pool():
+    # With power-of-two scales every code value * scale is exact in f32, so the
+    # FP8 decode must equal, bit for bit, the f32 decode (pinned above) over a
+    # pool holding those values. NaN codes in unused rows become NaN values there.
+    w, k8, v8, ks, vs = _fp8_workload(150, pow2_scales=True)
+    o8, l8 = _fp8_decode(w, k8, v8, ks, vs)
+    h = np.arange(w.num_kv_heads)[None, :, None, None]
+    k32 = (oracle.e4m3_values(k8) * ks[h]).astype(np.float32)
+    v32 = (oracle.e4m3_values(v8) * vs[h]).astype(np.float32)
+    q32 = oracle.decode_elements(w.q, "f16").astype(np.float32)
+    t = w.table
+    o32, l32 = oracle.paged_decode(q32, k32, v32, t.indices, t.indptr, t.last_page_len, w.num_qo_heads,
+                                   w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale, "f32")
+    assert np.array_equal(o8, o32) and np.array_equal(l8, l32)
+
+
+def test_fp8_scales_act_per_kv_head():
+    # v_scale[h] scales the outputs of kv head h's q heads and nothing else;
+    # k_scale[h] acts like sm_scale for those heads.
+    w, k8, v8, ks, vs = _fp8_workload(151, q_dtype="bf16")
+    g = w.num_qo_heads // w.num_kv_heads
+    o, l = _fp8_decode(w, k8, v8, ks, vs)
+    vs2 = vs.copy()
+    vs2[1] *= 2
+    o2, l2 = _fp8_decode(w, k8, v8, ks, vs2)
+    np.testing.assert_allclose(o2[:, g:2 * g], 2 * o[:, g:2 * g], rtol=1e-14, atol=0)
+    assert np.array_equal(o2[:, :g], o[:, :g]) and np.array_equal(l2, l)
+    ks3 = np.full_like(ks, ks[0])
+    o3, l3 = _fp8_decode(w, k8, v8, ks3, vs, sm_scale=np.float32(w.sm_scale * 2))
+    ks4 = np.full_like(ks, 2 * ks[0])
+    o4, l4 = _fp8_decode(w, k8, v8, ks4, vs)
+    np.testing.assert_allclose(o3, o4, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l3, l4, rtol=1e-12, atol=1e-14)
+
+
+def test_fp8_append_rounds_the_f32_quotient():
+    w, k8, v8, ks, vs = _fp8_workload(152, lens=(3, 16, 40))
+    t = wl.table_after_append(w.table)
+    kn, vn = w.new_rows(0)
+    kb, vb = k8.copy(), v8.copy()
+    oracle.paged_append_fp8(kn, vn, ks, vs, k8, v8, t.indices, t.indptr, t.last_page_len, "f16")
+    kx = oracle.decode_elements(kn, "f16").astype(np.float32)
+    changed = 0
+    for b in range(w.batch):
+        page = t.indices[t.indptr[b + 1] - 1]
+        slot = t.last_page_len[b] - 1
+        for h in range(w.num_kv_heads):
+            quot = kx[b, h] / ks[h]  # f32 division
+            got = k8[page, h, slot]
+            err = np.abs(oracle.e4m3_values(got) - quot.astype(np.float64))
+            # no other code is nearer to the quotient
+            allv = oracle.e4m3_values(np.arange(256, dtype=np.uint8))
+            best = np.nanmin(np.abs(allv[None, :] - quot.astype(np.float64)[:, None]), axis=1)
+            assert np.all(err <= best)
+            kb[page, h, slot] = got
+            changed += 1
+    assert np.array_equal(k8, kb)  # nothing but the new slots changed
+    assert changed == w.batch * w.num_kv_heads
+    assert not np.array_equal(v8, vb)

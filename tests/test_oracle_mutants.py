@@ -22,6 +22,8 @@ MUTANTS = {
     9: "merge weights exp(L - lse_c) instead of exp(lse_c - L)",
     10: "contiguous append one row early",
     11: "NHD cache addressed as HND",
+    12: "E4M3 exponent bias 8 instead of 7",
+    13: "FP8 V scaled by the K scale",
 }
 
 

@@ -38,7 +38,7 @@ ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
 _NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
 
 # Stream ids: each tensor of a workload draws from its own splitmix64 stream.
-STREAMS = {"q": 1, "k": 2, "v": 3, "k_new": 4, "v_new": 5}
+STREAMS = {"q": 1, "k": 2, "v": 3, "k_new": 4, "v_new": 5, "k_e4m3": 6, "v_e4m3": 7, "k_scale": 8, "v_scale": 9}
 
 
 def build(force: bool = False) -> str:
@@ -64,6 +64,9 @@ def _lib():
         lib.wl_fill_normal.restype = ctypes.c_int
         lib.wl_round_f32.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64]
         lib.wl_round_f32.restype = ctypes.c_int
+        lib.wl_fill_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                     ctypes.c_int, ctypes.c_int]
+        lib.wl_fill_e4m3.restype = ctypes.c_int
         lib.wl_splitmix64_at.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         lib.wl_splitmix64_at.restype = ctypes.c_uint64
         _lib_handle = lib
@@ -111,7 +114,39 @@ def round_f32(values: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def nan_value(dtype: str):
+    if dtype == "e4m3":
+        return np.uint8(E4M3_NAN)
     return np.float32(np.nan) if dtype == "f32" else np.uint16(_NAN_BITS[dtype])
+
+
+# --- FP8 (E4M3) pools -----------------------------------------------------------------------
+
+E4M3_NAN = 0x7F  # S.1111.111 with S = 0
+
+
+def e4m3_codes(shape, key: int, first: int = 0, e_lo: int = 4, e_hi: int = 9) -> np.ndarray:
+    """Random E4M3 codes (uint8): random sign and mantissa, exponent field uniform in
+    [e_lo, e_hi] (default: magnitudes 0.125 .. 7.5). Bit fields only, no rounding."""
+    out = np.empty(shape, dtype=np.uint8)
+    if _lib().wl_fill_e4m3(out.ctypes.data, out.size, key, first, e_lo, e_hi) != 0:
+        raise ValueError("wl_fill_e4m3: exponent range must lie in [1, 14]")
+    return out
+
+
+def kv_scales(num_kv_heads: int, key: int, lo: float = 0.05, hi: float = 0.2) -> np.ndarray:
+    """Per-kv-head float32 scales lo + (hi - lo) * u, u uniform from stream `key`."""
+    u = np.array([(splitmix64_at(key, h) >> 11) / float(1 << 53) for h in range(num_kv_heads)])
+    return (lo + (hi - lo) * u).astype(np.float32)
+
+
+def fp8_pool(w: "Workload"):
+    """An E4M3 pool of w's shape and table: codes from their own streams, unused
+    rows poisoned with the NaN code, and per-kv-head K and V scales."""
+    k = e4m3_codes(w.k_data.shape, stream_key(w.seed, "k_e4m3"))
+    v = e4m3_codes(w.v_data.shape, stream_key(w.seed, "v_e4m3"))
+    poison_unused(k, v, w.table, "e4m3")
+    return (k, v, kv_scales(w.num_kv_heads, stream_key(w.seed, "k_scale")),
+            kv_scales(w.num_kv_heads, stream_key(w.seed, "v_scale")))
 
 
 @dataclass

@@ -121,5 +121,22 @@ int wl_round_f32(const float* in, uint16_t* out, int dtype, uint64_t n) {
     return 0;
 }
 
+/*
+ * Random FP8 E4M3 codes: element i of stream `key` takes the bits of splitmix64
+ * output i: sign = bit 0, exponent field = e_lo + (bits 1.. mod (e_hi - e_lo + 1)),
+ * mantissa = bits 8..10. Only bit fields are drawn, never a rounding: with
+ * 1 <= e_lo <= e_hi <= 14 no NaN code and no subnormal can occur.
+ */
+int wl_fill_e4m3(uint8_t* out, uint64_t n, uint64_t key, uint64_t first, int e_lo, int e_hi) {
+    if (e_lo < 1 || e_hi > 14 || e_lo > e_hi) return 1;
+    const uint64_t span = (uint64_t)(e_hi - e_lo + 1);
+    for (uint64_t i = 0; i < n; ++i) {
+        const uint64_t r = sm64_at(key, first + i);
+        const unsigned e = (unsigned)e_lo + (unsigned)((r >> 1) % span);
+        out[i] = (uint8_t)(((r & 1u) << 7) | (e << 3) | ((r >> 8) & 7u));
+    }
+    return 0;
+}
+
 /* One splitmix64 output, exposed so a test can check the generator itself. */
 uint64_t wl_splitmix64_at(uint64_t key, uint64_t n) { return sm64_at(key, n); }
