@@ -139,19 +139,30 @@ def load_workload(name: str, rank: int = 0):
         return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous"
     if name == "long_context_nhd":
         return wl.long_context_f16(seed=1002 + 100 * rank), "contiguous_nhd"
+    if name == "llama3_8b_fp8":
+        return wl.llama3_8b_bf16(seed=1001 + 100 * rank), "paged_fp8"
     return wl.CONFIGS[name](seed=wl.CONFIGS[name].__defaults__[0] + 100 * rank), "paged"
 
 
-def decode_kernel_name(w) -> str:
+def decode_kernel_name(w, mode: str = "paged") -> str:
     """The decode kernel the library picks for this workload (tensor cores for
-    16-bit tiles of 5..8 q heads per kv head, CUDA cores otherwise)."""
+    16-bit tiles of 5..8 q heads per kv head, CUDA cores otherwise and for
+    E4M3 pools)."""
+    if mode == "paged_fp8":
+        return "decode_kernel"
     g = w.group
     tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
     per_tile = g // tiles
     return "decode_mma_kernel" if (w.dtype != "f32" and per_tile > 4) else "decode_kernel"
 
 
-def algorithmic_bytes(w, table=None) -> int:
+def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:
+    """K and V rows read (one byte per element for E4M3 pools, plus the two
+    scale vectors), q read and o written."""
+    if mode == "paged_fp8":
+        import workloads as wl
+
+        return w.kv_bytes(table) // wl.ELEM_BYTES[w.dtype] + 2 * 4 * w.num_kv_heads + w.qo_bytes()
     return w.kv_bytes(table) + w.qo_bytes()
 
 
@@ -199,6 +210,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         def step(i):
             decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
         bytes_per_step = [algorithmic_bytes(w)]
+        decode_bytes_per_step = bytes_per_step
+    elif mode == "paged_fp8":
+        k8, v8, ks, vs = wl.fp8_pool(w)
+        k, v = torch.from_numpy(k8).to(dev), torch.from_numpy(v8).to(dev)
+        ksd, vsd = torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)
+        del k8, v8
+        ws = pd.alloc_workspace(pd.pd_paged_decode_fp8_workspace_bytes(
+            w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, code), dev)
+        ind, ptr, lpl = table_dev(w.table, dev)
+
+        def step(i):
+            pd.pd_paged_decode_fp8(q, k, v, ksd, vsd, ind, ptr, lpl, o, lse, w.sm_scale, ws)
+        bytes_per_step = [algorithmic_bytes(w, mode=mode)]
         decode_bytes_per_step = bytes_per_step
     else:
         k = to_dev(w.k_data, w.dtype, dev)
@@ -397,10 +421,16 @@ def cpu_baseline(w, mode: str, budget_s: float = 12.0) -> dict:
         kc, vc, nv = wl.contiguous_copy(w)
         if layout == "nhd":
             kc, vc = np.ascontiguousarray(kc.transpose(0, 2, 1, 3)), np.ascontiguousarray(vc.transpose(0, 2, 1, 3))
+    if mode == "paged_fp8":
+        k8, v8, ks, vs = wl.fp8_pool(w)
     n, t0 = 0, time.perf_counter()
     while True:
         if mode.startswith("contiguous"):
             oracle.contiguous_decode(w.q, kc, vc, w.num_qo_heads, nv, w.sm_scale, w.dtype, threads, layout=layout)
+        elif mode == "paged_fp8":
+            t = w.table
+            oracle.paged_decode_fp8(w.q, k8, v8, ks, vs, t.indices, t.indptr, t.last_page_len, w.num_qo_heads,
+                                    w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale, w.dtype, threads)
         else:
             oracle.paged_decode_workload(w, table=table, threads=threads)
         n += 1
@@ -408,7 +438,7 @@ def cpu_baseline(w, mode: str, budget_s: float = 12.0) -> dict:
         if el >= budget_s or (n >= 1 and el * (n + 1) / n > 3 * budget_s):
             break
     per = el / n
-    value = algorithmic_bytes(w, table) / per / 1e12
+    value = algorithmic_bytes(w, table, mode) / per / 1e12
     return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"full {w.name} decode, {n} call(s), {per * 1e3:.1f} ms per call on {threads} threads"}
 
@@ -419,8 +449,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG,
-                    choices=["tiny", "llama3_8b", "long_context", "long_context_contiguous", "long_context_nhd",
-                             "ragged_70b", "mha_append"])
+                    choices=["tiny", "llama3_8b", "llama3_8b_fp8", "long_context", "long_context_contiguous",
+                             "long_context_nhd", "ragged_70b", "mha_append"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--append", default="fused", choices=["fused", "separate"],
                     help="append workloads: one fused append + decode launch, or an append launch then a decode")
@@ -440,10 +470,11 @@ def main():
         for _ in range(args.warmup):
             pass  # the oracle has no warm state; warm-up calls would only repeat the timing
         cb = cpu_baseline(w, mode, budget_s=max(5.0, min(60.0, 2.0 * args.steps)))
-        per_ms = algorithmic_bytes(w) / (cb["value"] * 1e12) * 1e3
+        per_ms = algorithmic_bytes(w, mode=mode) / (cb["value"] * 1e12) * 1e3
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if mode == "paged_fp8" else w.dtype,
+                "data": "synthetic",
                 "config": {"workload": w.name}, "cpu_baseline": cb,
                 "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -467,9 +498,9 @@ def main():
     dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
     dec_bytes = r["decode_bytes_mean"]  # the decode kernel's own bytes (no append rows)
     achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
-    kname = decode_kernel_name(w)
-    traffic = recorded_traffic(kname, w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd"}
-                                                .get(r["mode"], "")))
+    kname = decode_kernel_name(w, r["mode"])
+    traffic = recorded_traffic(kname, w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd",
+                                                 "paged_fp8": "/e4m3"}.get(r["mode"], "")))
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
                 "peak_source": peaks["source"], "kernel": kname,
@@ -484,7 +515,7 @@ def main():
     line = {
         "metric": METRIC, "value": tbps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if r["mode"] == "paged_fp8" else w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "mode": r["mode"] + (f", append {args.append}" if w.append_steps else ""),
                    "batch": w.batch, "num_qo_heads": w.num_qo_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,

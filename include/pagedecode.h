@@ -140,6 +140,42 @@ pd_status pd_paged_append(const void* k_new, const void* v_new, void* k_data, vo
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 KV pools. This is an extension of this library, not a layout of the
+ * pages above: K and V pages hold one-byte E4M3 codes, in the same HND layout
+ * as pd_paged_decode ([max_num_pages, num_kv_heads, page_size, head_dim]), and
+ * element value = E4M3 value of the code * k_scale[h] (v_scale[h] for V), h
+ * its kv head. E4M3 is the format of the OCP 8-bit floating point
+ * specification (bias 7, 3 mantissa bits, S.1111.111 NaN, largest finite 448).
+ * The pool is half the bytes of an f16 pool, and this decode is bound by
+ * those bytes.
+ *
+ * pd_paged_decode_fp8: the arguments of pd_paged_decode plus k_scale, v_scale
+ *   (device f32 [num_kv_heads], 4-byte aligned); dtype (PD_F16 or PD_BF16) is
+ *   the type of q and o. The workspace size comes from
+ *   pd_paged_decode_fp8_workspace_bytes (the stage geometry differs from the
+ *   16-bit pools). Results, lse and errors as pd_paged_decode.
+ * pd_paged_append_fp8: the slot of pd_paged_append receives, for each element
+ *   x of k_new (v_new), the code of x / k_scale[h] (v_scale[h]): x widened to
+ *   f32, the division in f32, rounded to the nearest code with ties to even,
+ *   saturating at +-448 (NaN stays NaN). dtype is the type of k_new / v_new
+ *   (PD_F16 or PD_BF16). Table errors as pd_paged_append.
+ */
+size_t pd_paged_decode_fp8_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                           pd_dtype dtype);
+pd_status pd_paged_decode_fp8(const void* q, const void* k_data, const void* v_data, const float* k_scale,
+                              const float* v_scale, const int32_t* indices, const int32_t* indptr,
+                              const int32_t* last_page_len, void* o, float* lse, int batch,
+                              int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                              int num_total_pages, int num_indices, float sm_scale, pd_dtype dtype,
+                              void* workspace, size_t workspace_bytes, void* stream);
+pd_status pd_paged_append_fp8(const void* k_new, const void* v_new, const float* k_scale,
+                              const float* v_scale, void* k_data, void* v_data, const int32_t* indices,
+                              const int32_t* indptr, const int32_t* last_page_len, int batch,
+                              int num_kv_heads, int head_dim, int page_size, int num_total_pages,
+                              int num_indices, pd_dtype dtype, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Append, then decode, in one kernel launch. The companion plans of
  * batch_paged_decode.rs (module doc "Companion plans": PagedKvAppendPlan, then
  * BatchPagedDecodePlan) run as two plans per decode step; this call gives

@@ -54,6 +54,10 @@ _SIGS = {
     "pd_paged_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _P, _S, _P]),
     "pd_contiguous_append_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "pd_paged_decode_fp8_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
+    "pd_paged_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
+                                 _P]),
+    "pd_paged_append_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _S, _P]),
     "pd_contiguous_decode_nhd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "pd_contiguous_append_nhd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pd_contiguous_append_decode_nhd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
@@ -285,3 +289,37 @@ def pd_contiguous_append_decode_nhd(q, k_new, v_new, k_cache, v_cache, o, lse, p
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(o),
         _ptr(lse) if lse is not None else None, batch, num_qo_heads, num_kv_heads, head_dim, max_kv_len,
         int(position), float(sm_scale), _dtype_code(q), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+# --- FP8 (E4M3) pools: k_data, v_data uint8 [pages, Hk, page_size, D]; scales f32 [Hk] ---------
+
+def pd_paged_decode_fp8_workspace_bytes(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                                        dtype: int) -> int:
+    n = _lib.pd_paged_decode_fp8_workspace_bytes(batch, num_qo_heads, num_kv_heads, head_dim, dtype)
+    if n == 0:
+        raise PagedecodeError(PD_ERR_INVALID, pd_last_error_string())
+    return n
+
+
+def pd_paged_decode_fp8(q, k_data, v_data, k_scale, v_scale, indices, indptr, last_page_len, o, lse,
+                        sm_scale: float, workspace, stream=None) -> None:
+    """q, o [batch, Hq, D] f16/bf16; k_data, v_data uint8 E4M3 [pages, Hk, page_size, D]; scales f32 [Hk]."""
+    batch, num_qo_heads, head_dim = q.shape
+    num_total_pages, num_kv_heads, page_size, _ = k_data.shape
+    _check(_lib.pd_paged_decode_fp8(
+        _ptr(q), _ptr(k_data), _ptr(v_data), _ptr(k_scale), _ptr(v_scale),
+        _ptr(indices) if indices.numel() else None, _ptr(indptr), _ptr(last_page_len), _ptr(o), _ptr(lse), batch,
+        num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, indices.numel(), float(sm_scale),
+        _dtype_code(q), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def pd_paged_append_fp8(k_new, v_new, k_scale, v_scale, k_data, v_data, indices, indptr, last_page_len, workspace,
+                        stream=None) -> None:
+    """Quantise k_new, v_new [batch, Hk, D] (f16/bf16) into their slots of the E4M3 pools."""
+    batch, num_kv_heads, head_dim = k_new.shape
+    num_total_pages, _, page_size, _ = k_data.shape
+    _check(_lib.pd_paged_append_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(k_scale), _ptr(v_scale), _ptr(k_data), _ptr(v_data),
+        _ptr(indices) if indices.numel() else None, _ptr(indptr), _ptr(last_page_len), batch, num_kv_heads,
+        head_dim, page_size, num_total_pages, indices.numel(), _dtype_code(k_new), _ptr(workspace),
+        workspace.numel(), _stream(stream)))

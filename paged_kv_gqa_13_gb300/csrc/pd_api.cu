@@ -25,6 +25,8 @@ PD_VARIANTS(f32)
 PD_VARIANTS(f16)
 PD_VARIANTS(bf16)
 #undef PD_VARIANTS
+bool lookup_fp8_f16(int head_dim, int heads, KernelSet* ks);
+bool lookup_fp8_bf16(int head_dim, int heads, KernelSet* ks);
 }  // namespace pd
 
 namespace {
@@ -66,6 +68,15 @@ bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
 #undef PD_LOOKUP
     }
     return false;
+}
+
+// Kernels for an E4M3 pool with q / o of type dt (f16 or bf16).
+bool lookup_fp8(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
+    switch (dt) {
+        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fp8_f16(D, G, ks);
+        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fp8_bf16(D, G, ks);
+        default: return false;
+    }
 }
 
 // Per-device facts, read once.
@@ -135,16 +146,17 @@ void split_group(int g, int* tiles, int* per) {
     *per = g / t;
 }
 
-pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p);
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, Plan* p);
 
 // Plans depend only on the shape and the device: keep the last few so that a
 // decode loop pays the occupancy query and the attribute set-up once.
-pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p) {
+// fp8: the K/V pool holds E4M3 codes (dt is then the type of q and o).
+pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p, bool fp8 = false) {
     struct Entry {
         int dev;
         pd_dtype dt;
         int batch, Hq, Hk, D;
-        bool contiguous;
+        bool contiguous, fp8;
         Plan plan;
     };
     static Entry cache[16];
@@ -156,22 +168,22 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
         for (int i = 0; i < used; ++i) {
             const Entry& e = cache[i];
             if (e.dev == dev && e.dt == dt && e.batch == batch && e.Hq == Hq && e.Hk == Hk && e.D == D &&
-                e.contiguous == contiguous) {
+                e.contiguous == contiguous && e.fp8 == fp8) {
                 *p = e.plan;
                 return PD_OK;
             }
         }
     }
-    const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, p);
+    const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, fp8, p);
     if (st != PD_OK) return st;
     std::lock_guard<std::mutex> lk(g_mu);
-    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, *p};
+    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, fp8, *p};
     next = (next + 1) % 16;
     if (used < 16) ++used;
     return PD_OK;
 }
 
-pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p) {
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, Plan* p) {
     if (dt != PD_F32 && dt != PD_F16 && dt != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || Hq <= 0 || Hk <= 0) return fail(PD_ERR_INVALID, "batch, num_qo_heads and num_kv_heads must be positive");
     if (Hq % Hk != 0) return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", Hq, Hk);
@@ -180,7 +192,9 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     split_group(p->group, &p->head_tiles, &p->heads_per_tile);
     p->G = 1;
     while (p->G < p->heads_per_tile) p->G *= 2;
-    if (!lookup(dt, D, p->G, &p->ks)) return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
+    if (fp8 && dt == PD_F32) return fail(PD_ERR_UNSUPPORTED, "E4M3 pools take f16 or bf16 q and o");
+    if (!(fp8 ? lookup_fp8(dt, D, p->G, &p->ks) : lookup(dt, D, p->G, &p->ks)))
+        return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
     DeviceInfo di;
     pd_status st = device_info(&di);
     if (st != PD_OK) return st;
@@ -193,6 +207,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     // share its layout; size one wave by the lowest of their occupancies.
     int per_sm = 1 << 30;
     for (int v = 0; v < (contiguous ? 4 : 2); ++v) {
+        if (p->ks.variant[v] == nullptr) continue;
         if ((st = allow_smem(p->ks.variant[v], int(p->smem))) != PD_OK) return st;
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, p->ks.variant[v], p->nwarps * 32, p->smem);
@@ -406,6 +421,57 @@ __global__ void __launch_bounds__(128) append_kernel(const uint8_t* k_new, const
     }
 }
 
+// E4M3 pool: one warp per (request, kv head) writes the codes of the new K and
+// V rows into their slot (the table checks of append_kernel): code =
+// E4M3(x / scale[kv head]), x widened to f32, the division in f32 (IEEE,
+// rounded to nearest), the conversion rounding to nearest even and
+// saturating at +-448.
+template <typename T>
+__global__ void __launch_bounds__(128) append_fp8_kernel(const T* k_new, const T* v_new, const float* k_scale,
+                                                         const float* v_scale, uint8_t* k_data, uint8_t* v_data,
+                                                         const int32_t* indices, const int32_t* indptr,
+                                                         const int32_t* last_page_len, int batch, int Hk, int D,
+                                                         int page_size, int num_total_pages, int num_indices,
+                                                         int* flags) {
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (w >= (long long)batch * Hk) return;
+    const int b = int(w / Hk), kh = int(w % Hk);
+    const int lo = __ldg(indptr + b), hi = __ldg(indptr + b + 1);
+    if (hi <= lo || lo < 0 || hi > num_indices) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadIndptr);
+        return;
+    }
+    const int page = __ldg(indices + hi - 1);
+    const int slot = __ldg(last_page_len + b) - 1;
+    if (page < 0 || page >= num_total_pages) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadPage);
+        return;
+    }
+    if (slot < 0 || slot >= page_size) {
+        if (lane == 0 && kh == 0) atomicOr(flags, pd::kFlagBadLastPageLen);
+        return;
+    }
+    const size_t dst = ((size_t(page) * Hk + kh) * page_size + slot) * size_t(D);
+    const size_t src = (size_t(b) * Hk + kh) * size_t(D);
+    const float ks = __ldg(k_scale + kh), vs = __ldg(v_scale + kh);
+    for (int e = lane * 8; e < D; e += 32 * 8) {
+        float fk[8], fv[8];
+        pd::Elt<T>::to_f32(__ldg(reinterpret_cast<const uint4*>(k_new + src + e)), fk);
+        pd::Elt<T>::to_f32(__ldg(reinterpret_cast<const uint4*>(v_new + src + e)), fv);
+        uint32_t ck[2] = {0, 0}, cv[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 qk = make_float2(__fdiv_rn(fk[2 * i], ks), __fdiv_rn(fk[2 * i + 1], ks));
+            const float2 qv = make_float2(__fdiv_rn(fv[2 * i], vs), __fdiv_rn(fv[2 * i + 1], vs));
+            ck[i / 2] |= uint32_t(__nv_cvt_float2_to_fp8x2(qk, __NV_SATFINITE, __NV_E4M3)) << (16 * (i % 2));
+            cv[i / 2] |= uint32_t(__nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3)) << (16 * (i % 2));
+        }
+        *reinterpret_cast<uint2*>(k_data + dst + e) = make_uint2(ck[0], ck[1]);
+        *reinterpret_cast<uint2*>(v_data + dst + e) = make_uint2(cv[0], cv[1]);
+    }
+}
+
 // One warp per (request, kv head): copy the new K and V rows into token
 // `position` of the contiguous cache, HND [b, Hk, max_kv_len, D] or NHD
 // [b, max_kv_len, Hk, D].
@@ -472,13 +538,16 @@ size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num
     return p.ws_bytes;
 }
 
-// The paged decode, with the fused append when k_new / v_new are not null.
+// The paged decode, with the fused append when k_new / v_new are not null,
+// over an E4M3 pool when k_scale / v_scale are not null.
 static pd_status paged_decode_impl(const void* q, const void* k_new, const void* v_new, const void* k_data,
                                    const void* v_data, const int32_t* indices, const int32_t* indptr,
                                    const int32_t* last_page_len, void* o, float* lse, int batch, int num_qo_heads,
                                    int num_kv_heads, int head_dim, int page_size, int num_total_pages,
                                    int num_indices, float sm_scale, pd_dtype dtype, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+                                   size_t workspace_bytes, void* stream, const float* k_scale = nullptr,
+                                   const float* v_scale = nullptr) {
+    const bool fp8 = k_scale != nullptr;
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0)
         return fail(PD_ERR_INVALID, "batch, num_qo_heads, num_kv_heads, page_size and num_total_pages must be positive");
@@ -495,7 +564,7 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     if (!aligned(lse, 4) || !aligned(indptr, 4) || !aligned(last_page_len, 4) || (indices && !aligned(indices, 4)))
         return fail(PD_ERR_UNSUPPORTED, "lse, indices, indptr and last_page_len must be 4-byte aligned");
     Plan pl;
-    pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl);
+    pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl, fp8);
     if (st != PD_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, pl.ws_bytes)) != PD_OK) return st;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -503,6 +572,8 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     a.q = q;
     a.k = k_data;
     a.v = v_data;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.indices = indices;
     a.indptr = indptr;
     a.last_page_len = last_page_len;
@@ -538,6 +609,27 @@ pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data,
     return paged_decode_impl(q, nullptr, nullptr, k_data, v_data, indices, indptr, last_page_len, o, lse, batch,
                              num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale,
                              dtype, workspace, workspace_bytes, stream);
+}
+
+size_t pd_paged_decode_fp8_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                           pd_dtype dtype) {
+    Plan p;
+    if (make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &p, true) != PD_OK) return 0;
+    ok();
+    return p.ws_bytes;
+}
+
+pd_status pd_paged_decode_fp8(const void* q, const void* k_data, const void* v_data, const float* k_scale,
+                              const float* v_scale, const int32_t* indices, const int32_t* indptr,
+                              const int32_t* last_page_len, void* o, float* lse, int batch, int num_qo_heads,
+                              int num_kv_heads, int head_dim, int page_size, int num_total_pages, int num_indices,
+                              float sm_scale, pd_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "E4M3 pools take PD_F16 or PD_BF16 q and o");
+    if (!k_scale || !v_scale) return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_scale, 4) || !aligned(v_scale, 4)) return fail(PD_ERR_UNSUPPORTED, "k_scale and v_scale must be 4-byte aligned");
+    return paged_decode_impl(q, nullptr, nullptr, k_data, v_data, indices, indptr, last_page_len, o, lse, batch,
+                             num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale,
+                             dtype, workspace, workspace_bytes, stream, k_scale, v_scale);
 }
 
 pd_status pd_paged_append_decode(const void* q, const void* k_new, const void* v_new, void* k_data, void* v_data,
@@ -713,6 +805,47 @@ static pd_status contiguous_append_impl(const void* k_new, const void* v_new, vo
     cudaError_t e = cudaGetLastError();
     if (prof) mark(&g_prof.append_marks, s);
     if (e != cudaSuccess) return cuda_fail(e, "contiguous append launch");
+    return ok();
+}
+
+pd_status pd_paged_append_fp8(const void* k_new, const void* v_new, const float* k_scale, const float* v_scale,
+                              void* k_data, void* v_data, const int32_t* indices, const int32_t* indptr,
+                              const int32_t* last_page_len, int batch, int num_kv_heads, int head_dim, int page_size,
+                              int num_total_pages, int num_indices, pd_dtype dtype, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "k_new and v_new must be PD_F16 or PD_BF16");
+    if (batch <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0 || num_indices < 0)
+        return fail(PD_ERR_INVALID, "batch, num_kv_heads, page_size and num_total_pages must be positive");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    if (!k_new || !v_new || !k_scale || !v_scale || !k_data || !v_data || !indptr || !last_page_len ||
+        (num_indices > 0 && !indices))
+        return fail(PD_ERR_INVALID, "null pointer argument");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_data, 16) || !aligned(v_data, 16) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return fail(PD_ERR_UNSUPPORTED, "k_new, v_new, k_data, v_data must be 16-byte and the scales 4-byte aligned");
+    pd_status st = check_workspace(workspace, workspace_bytes, PD_WORKSPACE_HEADER_BYTES);
+    if (st != PD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long warps = (long long)batch * num_kv_heads;
+    std::unique_lock<std::mutex> plk(g_prof_mu);
+    const bool prof = g_prof.on;
+    if (!prof) plk.unlock();
+    if (prof) mark(&g_prof.append_marks, s);
+    const unsigned grid = unsigned((warps + 3) / 4);
+    if (dtype == PD_F16)
+        append_fp8_kernel<__half><<<grid, 128, 0, s>>>(
+            static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), k_scale, v_scale,
+            static_cast<uint8_t*>(k_data), static_cast<uint8_t*>(v_data), indices, indptr, last_page_len, batch,
+            num_kv_heads, head_dim, page_size, num_total_pages, num_indices, static_cast<int*>(workspace));
+    else
+        append_fp8_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), k_scale, v_scale,
+            static_cast<uint8_t*>(k_data), static_cast<uint8_t*>(v_data), indices, indptr, last_page_len, batch,
+            num_kv_heads, head_dim, page_size, num_total_pages, num_indices, static_cast<int*>(workspace));
+    cudaError_t e = cudaGetLastError();
+    if (prof) mark(&g_prof.append_marks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 append launch");
     return ok();
 }
 

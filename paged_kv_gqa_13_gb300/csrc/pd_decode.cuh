@@ -37,7 +37,9 @@ constexpr int kStages = 3;
 constexpr int kChunkBytes = 4096;  // K bytes of one stage (V the same)
 constexpr float kTau = 8.0f;       // reference max slack, log2 units: p <= 2^kTau
 
-template <typename T, int D, int G>
+// KvEsz: bytes per K/V element (sizeof(T), or 1 for E4M3 pools). q, o and
+// the lane-to-column map follow T either way.
+template <typename T, int D, int G, int KvEsz = int(sizeof(T))>
 struct Cfg {
     static constexpr int kEsz = int(sizeof(T));
     static constexpr int kVec = 16 / kEsz;           // elements per 16-byte vector
@@ -45,8 +47,9 @@ struct Cfg {
     static constexpr int kNvec = kEpl / kVec;        // vectors per lane per row
     static constexpr int kL = D / kEpl;              // lanes per row
     static constexpr int kRW = 32 / kL;              // rows side by side in a warp
-    static constexpr int kRowBytes = D * kEsz;
-    static constexpr int kRC = kChunkBytes / kRowBytes;  // rows per stage
+    static constexpr int kRowBytes = D * kEsz;            // q / o row
+    static constexpr int kKvRowBytes = D * KvEsz;         // K / V row
+    static constexpr int kRC = kChunkBytes / kKvRowBytes;  // rows per stage
     static constexpr int kRR0 = (16 / G) > 0 ? (16 / G) : 1;
     static constexpr int kRR = kRR0 < (kRC / kRW) ? kRR0 : (kRC / kRW);  // rows per row group per round
     static constexpr int kRounds = kRC / (kRW * kRR);
@@ -72,7 +75,9 @@ template <typename T, int D, int G, int kVariant>
 __global__ void __launch_bounds__(256, 1)
     decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kFused = (kVariant & kVarFused) != 0, kNhd = (kVariant & kVarNhd) != 0;
-    using C = Cfg<T, D, G>;
+    constexpr bool kFp8 = (kVariant & kVarFp8) != 0;
+    static_assert(!kFp8 || (sizeof(T) == 2 && !kFused && !kNhd), "E4M3 pools: 16-bit q / o, paged, no fused append");
+    using C = Cfg<T, D, G, kFp8 ? 1 : int(sizeof(T))>;
     using E = Elt<T>;
     constexpr int kL = C::kL, kRW = C::kRW, kRR = C::kRR, kV = C::kV, kVF = C::kVF;
     constexpr int kVec = C::kVec, kNvec = C::kNvec, kEpl = C::kEpl, kRC = C::kRC;
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
         }
-        walk.template prefetch_first_slabs<kNhd>(first_page, kStages, size_t(C::kRowBytes));
+        walk.template prefetch_first_slabs<kNhd>(first_page, kStages, size_t(C::kKvRowBytes));
     });
     __syncthreads();  // the only block-wide barrier: warps are independent from here on
     // Let the merge kernel be scheduled now; it waits for this grid before it
@@ -125,7 +130,8 @@ __global__ void __launch_bounds__(256, 1)
     walk.build(p0, first_page);
 
     const uint64_t policy = l2_evict_first_policy();
-    const size_t row_bytes = size_t(C::kRowBytes);
+    const size_t row_bytes = size_t(C::kRowBytes);       // q
+    const size_t kv_row_bytes = size_t(C::kKvRowBytes);  // K, V
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot) {
         Chunk ck;
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
         if constexpr (kFused) {
-            if (have && (ck.flags & kAppendRow)) write_new_row<kNhd>(a, ck, lane, row_bytes);
+            if (have && (ck.flags & kAppendRow)) write_new_row<kNhd>(a, ck, lane, kv_row_bytes);
         }
         if (lane != 0) return;
         if (!have) {
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(256, 1)
         meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
         // An NHD box lands whole: kRC rows, those past the valid length as zeros.
         const uint32_t kv_bytes =
-            kNhd ? (ck.rows > 0 ? uint32_t(kChunkBytes) : 0u) : uint32_t(ck.rows) * uint32_t(row_bytes);
+            kNhd ? (ck.rows > 0 ? uint32_t(kChunkBytes) : 0u) : uint32_t(ck.rows) * uint32_t(kv_row_bytes);
         const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * C::kRowBytes) : 0u;
         const uint32_t total = 2 * kv_bytes + q_bytes;
         if (total == 0) {
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(256, 1)
                 tma_load_4d(smem_u32(st), &tmk, 0, ck.kh, ck.row0, ck.slab, bar, policy);
                 tma_load_4d(smem_u32(st + kChunkBytes), &tmv, 0, ck.kh, ck.row0, ck.slab, bar, policy);
             } else {
-                const size_t off = kv_row<false>(a, ck.slab, ck.kh, ck.row0) * row_bytes;
+                const size_t off = kv_row<false>(a, ck.slab, ck.kh, ck.row0) * kv_row_bytes;
                 bulk_g2s(smem_u32(st), static_cast<const uint8_t*>(a.k) + off, kv_bytes, bar, policy);
                 bulk_g2s(smem_u32(st + kChunkBytes), static_cast<const uint8_t*>(a.v) + off, kv_bytes, bar, policy);
             }
@@ -214,13 +220,15 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int kOwn = (kRW > 1) ? G * kEp2 / kRW : G * kEp2;  // float2 values a lane writes
     auto finalize = [&](int4 m) {
         float lh[G], inv[G];
+        // E4M3 pools: the V scale of this kv head is applied once, here.
+        const float vsc = kFp8 ? __ldg(a.v_scale + (m.z % a.num_qo_heads) / a.group) : 1.0f;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < kVF; ++j) s += (primary && hj[j] == h) ? lmy[j] : 0.f;
             lh[h] = warp_sum(s);
-            inv[h] = lh[h] > 0.f ? 1.0f / lh[h] : 0.f;
+            inv[h] = lh[h] > 0.f ? vsc / lh[h] : 0.f;
         }
         float2* flat = &acc[0][0];
         RSR::run(flat, lane);
@@ -262,6 +270,8 @@ __global__ void __launch_bounds__(256, 1)
         const uint8_t* vb = kb + kChunkBytes;
         if (m.y & kSegStart) {
             const uint8_t* qb = kb + 2 * kChunkBytes;
+            // E4M3 pools: the K scale of this kv head folds into q.
+            const float qs = kFp8 ? a.q_scale * __ldg(a.k_scale + (m.z % a.num_qo_heads) / a.group) : a.q_scale;
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(256, 1)
                     }
 #pragma unroll
                     for (int e = 0; e < kVec / 2; ++e)
-                        qf[h][nv * kVec / 2 + e] = make_float2(f[2 * e] * a.q_scale, f[2 * e + 1] * a.q_scale);
+                        qf[h][nv * kVec / 2 + e] = make_float2(f[2 * e] * qs, f[2 * e + 1] * qs);
                 }
         }
         const int rows = m.x;
@@ -294,7 +304,10 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int nv = 0; nv < kNvec; ++nv) {
                     float f[kVec];
-                    E::to_f32(*reinterpret_cast<const uint4*>(kb + r * C::kRowBytes + (nv * kL + c) * 16), f);
+                    if constexpr (kFp8)
+                        e4m3x8_to_f32(*reinterpret_cast<const uint2*>(kb + r * C::kKvRowBytes + (nv * kL + c) * 8), f);
+                    else
+                        E::to_f32(*reinterpret_cast<const uint4*>(kb + r * C::kKvRowBytes + (nv * kL + c) * 16), f);
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -366,7 +379,10 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int nv = 0; nv < kNvec; ++nv) {
                     float f[kVec];
-                    E::to_f32(*reinterpret_cast<const uint4*>(vb + r * C::kRowBytes + (nv * kL + c) * 16), f);
+                    if constexpr (kFp8)
+                        e4m3x8_to_f32(*reinterpret_cast<const uint2*>(vb + r * C::kKvRowBytes + (nv * kL + c) * 8), f);
+                    else
+                        E::to_f32(*reinterpret_cast<const uint4*>(vb + r * C::kKvRowBytes + (nv * kL + c) * 16), f);
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
                         const float2 p2 = make_float2(pv[rr * G + h], pv[rr * G + h]);

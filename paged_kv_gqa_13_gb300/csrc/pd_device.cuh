@@ -5,6 +5,7 @@
 
 #include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -192,6 +193,25 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ---------------------------------------------------------------- elements
 
+// Eight E4M3 codes (little-endian bytes of w) to f32. Every E4M3 value is an
+// f16 value, so the two steps through f16 are exact.
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float* f) {
+    const uint32_t h[2] = {w.x, w.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2_raw r =
+                __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h[i] >> (16 * j)), __NV_E4M3);
+            __half2 v;
+            memcpy(&v, &r, 4);
+            const float2 x = __half22float2(v);
+            f[4 * i + 2 * j] = x.x;
+            f[4 * i + 2 * j + 1] = x.y;
+        }
+    }
+}
+
 template <typename T>
 struct Elt;
 
@@ -364,6 +384,9 @@ struct DecodeArgs {
     // kernel then writes into k and v.
     const void* k_new;
     const void* v_new;
+    // FP8 pools (null otherwise): element value = E4M3 code value * scale[kv head].
+    const float* k_scale;
+    const float* v_scale;
 };
 
 struct MergeArgs {

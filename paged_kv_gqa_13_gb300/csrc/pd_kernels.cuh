@@ -59,10 +59,35 @@ bool lookup_variant_t(int D, int G, const void** fn) {
     constexpr bool kHalf = sizeof(T) == 2;
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
-        if constexpr (kHalf && GG == 8)                                                 \
+        if constexpr (kHalf && GG == 8 && (kVariant & kVarFp8) == 0)                    \
             *fn = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>);    \
         else                                                                            \
             *fn = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>);    \
+        return true;                                                                    \
+    }
+    PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)
+    PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)
+    PD_CASE(256, 1) PD_CASE(256, 2) PD_CASE(256, 4) PD_CASE(256, 8)
+#undef PD_CASE
+    return false;
+}
+
+// The decode kernel for E4M3 pools with q / o of type T (16-bit): the
+// CUDA-core decode at every group size, with its own stage geometry. The
+// merge kernels are those of T (from lookup_kernels_t), left untouched here.
+template <typename T>
+bool lookup_fp8_t(int D, int G, KernelSet* ks) {
+    static_assert(sizeof(T) == 2, "E4M3 pools take 16-bit q / o");
+#define PD_CASE(DD, GG)                                                                 \
+    if (D == DD && G == GG) {                                                           \
+        using C = Cfg<T, DD, GG, 1>;                                                    \
+        ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVarFp8>);  \
+        ks->warp_bytes = C::kWarpBytes;                                                 \
+        ks->rows_per_stage = C::kRC;                                                    \
+        ks->mma = 0;                                                                    \
+        ks->smem_slack = 0;                                                             \
+        ks->variant[0] = ks->decode;                                                    \
+        ks->variant[1] = ks->variant[2] = ks->variant[3] = nullptr;                     \
         return true;                                                                    \
     }
     PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)

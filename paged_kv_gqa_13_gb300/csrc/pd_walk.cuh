@@ -46,6 +46,7 @@ struct Chunk {
 // Variant bits of the decode kernels (compile-time, one instantiation each).
 constexpr int kVarFused = 1;  // the fused append (DecodeArgs::k_new set)
 constexpr int kVarNhd = 2;    // contiguous cache in NHD order [batch, max_kv_len, Hk, D]
+constexpr int kVarFp8 = 4;    // E4M3 K/V pools with per-kv-head scales (CUDA-core kernel, paged)
 
 // Index, in head_dim-element rows, of row `row` of kv head kh in slab `slab`:
 // HND [slab, kv head, row] (pages and the HND contiguous cache) or NHD

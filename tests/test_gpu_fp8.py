@@ -1,0 +1,117 @@
+"""GPU parity for FP8 (E4M3) pools with per-kv-head scales: the decode against
+the oracle's FP8 decode, the append bit-exact against the oracle's quantiser."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_helpers import compare, table_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CODE = {"f16": 1, "bf16": 2}
+
+
+class Fp8Device:
+    def __init__(self, w):
+        import torch
+
+        import paged_kv_gqa_13_gb300 as pd
+
+        self.w = w
+        self.k8, self.v8, self.ks, self.vs = wl.fp8_pool(w)
+        self.q = to_dev(w.q, w.dtype)
+        self.k = torch.from_numpy(self.k8).cuda()
+        self.v = torch.from_numpy(self.v8).cuda()
+        self.ksd = torch.from_numpy(self.ks).cuda()
+        self.vsd = torch.from_numpy(self.vs).cuda()
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device="cuda")
+        self.ws = pd.alloc_workspace(pd.pd_paged_decode_fp8_workspace_bytes(
+            w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, CODE[w.dtype]))
+        self.set_table(w.table)
+
+    def set_table(self, t):
+        self.t = t
+        self.ind, self.ptr, self.lpl = table_dev(t)
+
+    def decode(self):
+        import paged_kv_gqa_13_gb300 as pd
+
+        pd.pd_paged_decode_fp8(self.q, self.k, self.v, self.ksd, self.vsd, self.ind, self.ptr, self.lpl, self.o,
+                               self.lse, self.w.sm_scale, self.ws)
+        return self.o, self.lse
+
+    def oracle_decode(self, k8=None, v8=None):
+        t, w = self.t, self.w
+        return oracle.paged_decode_fp8(w.q, self.k8 if k8 is None else k8, self.v8 if v8 is None else v8, self.ks,
+                                       self.vs, t.indices, t.indptr, t.last_page_len, w.num_qo_heads,
+                                       w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale, w.dtype)
+
+
+LENS = [0, 1, 15, 16, 17, 100, 3000, 33]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hk,D,P", [
+    ("bf16", 32, 8, 128, 16),   # Llama-shaped group 4
+    ("f16", 32, 8, 128, 16),
+    ("bf16", 64, 8, 128, 32),   # group 8 (CUDA cores for E4M3)
+    ("f16", 16, 16, 256, 16),   # MHA, D 256
+    ("bf16", 16, 8, 64, 16),    # group 2, D 64
+    ("f16", 24, 2, 128, 8),     # group 12: two head tiles, page 8
+])
+def test_fp8_decode_matches_oracle(dtype, Hq, Hk, D, P):
+    w = wl.make_paged(f"fp8_{dtype}_{Hq}_{Hk}_{D}", dtype, LENS, Hq, Hk, D, P, seed=300 + Hq + D + P)
+    dev = Fp8Device(w)
+    o, lse = dev.decode()
+    compare(o, lse, *dev.oracle_decode(), dtype, "fp8 decode")
+    import paged_kv_gqa_13_gb300 as pd
+
+    assert pd.pd_read_device_flags(dev.ws) == 0
+
+
+@pytest.mark.parametrize("dtype,Hq,Hk,D", [("bf16", 32, 8, 128), ("f16", 16, 16, 256), ("f16", 8, 2, 64)])
+def test_fp8_append_then_decode(dtype, Hq, Hk, D):
+    import paged_kv_gqa_13_gb300 as pd
+
+    steps = 4
+    w = wl.make_paged(f"fp8a_{dtype}", dtype, [0, 15, 16, 31, 200], Hq, Hk, D, 16, seed=320 + Hq,
+                      extra_rows=steps, append_steps=steps)
+    dev = Fp8Device(w)
+    t = w.table
+    for step in range(steps):
+        t = wl.table_after_append(t)
+        kn, vn = w.new_rows(step)
+        dev.set_table(t)
+        pd.pd_paged_append_fp8(to_dev(kn, dtype), to_dev(vn, dtype), dev.ksd, dev.vsd, dev.k, dev.v, dev.ind,
+                               dev.ptr, dev.lpl, dev.ws)
+        oracle.paged_append_fp8(kn, vn, dev.ks, dev.vs, dev.k8, dev.v8, t.indices, t.indptr, t.last_page_len,
+                                dtype)
+        assert np.array_equal(dev.k.cpu().numpy(), dev.k8), f"K codes differ, step {step}"
+        assert np.array_equal(dev.v.cpu().numpy(), dev.v8), f"V codes differ, step {step}"
+        o, lse = dev.decode()
+        compare(o, lse, *dev.oracle_decode(), dtype, f"fp8 step {step}")
+    assert pd.pd_read_device_flags(dev.ws) == 0
+
+
+def test_fp8_append_saturates_and_rounds_ties_to_even():
+    """Chosen quotients: exact codes, midpoints between codes, and values past 448."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("fp8_sat", "f16", [5], 8, 2, 64, 16, seed=331, extra_rows=1)
+    dev = Fp8Device(w)
+    t = wl.table_after_append(w.table)
+    dev.set_table(t)
+    ks = np.array([1.0, 0.5], dtype=np.float32)
+    dev.ks, dev.ksd = ks, torch.from_numpy(ks).cuda()
+    x = np.zeros((1, 2, 64), dtype=np.float32)
+    x[0, :, :8] = [1.0, 1.0625, 1.125, 17.0, 448.0, 464.0, 1000.0, -0.0009765625]  # tie, tie, tie, ..., saturate
+    x[0, :, 8:16] = [2.0**-9, 3 * 2.0**-10, 240.0, 232.0, -232.0, 0.3, -7.0, 65504.0]
+    kn = wl.round_f32(x, "f16")
+    vn = kn.copy()
+    pd.pd_paged_append_fp8(to_dev(kn, "f16"), to_dev(vn, "f16"), dev.ksd, dev.vsd, dev.k, dev.v, dev.ind,
+                           dev.ptr, dev.lpl, dev.ws)
+    oracle.paged_append_fp8(kn, vn, dev.ks, dev.vs, dev.k8, dev.v8, t.indices, t.indptr, t.last_page_len, "f16")
+    assert np.array_equal(dev.k.cpu().numpy(), dev.k8) and np.array_equal(dev.v.cpu().numpy(), dev.v8)
