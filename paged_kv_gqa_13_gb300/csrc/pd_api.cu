@@ -195,6 +195,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     if (fp8 && dt == PD_F32) return fail(PD_ERR_UNSUPPORTED, "E4M3 pools take f16 or bf16 q and o");
     if (!(fp8 ? lookup_fp8(dt, D, p->G, &p->ks) : lookup(dt, D, p->G, &p->ks)))
         return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
+    p->G = p->ks.part_heads;  // the partial-result layout of the chosen kernel
     DeviceInfo di;
     pd_status st = device_info(&di);
     if (st != PD_OK) return st;

@@ -1,0 +1,375 @@
+// Batched decode attention over E4M3 (FP8) paged pools on tensor cores, for
+// tiles of 4..8 q heads per kv head at head_dim 128 / 256. Element value =
+// E4M3 code value * scale[kv head] (k_scale for K, v_scale for V).
+//
+// An E4M3 byte is a whole element, so per byte of HBM the arithmetic of the
+// group doubles against a 16-bit pool: the CUDA cores cannot keep up, and a
+// warp that moves one 16-row page per pipeline step spends more time on the
+// step's fixed work (barrier wait, walk, softmax bookkeeping) than the page's
+// bytes take to arrive. This kernel therefore:
+//  - stages up to two pages of the same segment per pipeline slot at head_dim
+//    128 (32 tokens, two independent 16-token score tiles), by 1-D bulk
+//    copies of the pages' contiguous rows;
+//  - builds the K operand of the score mma straight from the codes in shared
+//    memory, widening them in registers (every E4M3 value is an f16 value, so
+//    the f16 mma sees them exactly). The 16 dims of k step kk = 4j + t that
+//    lane (g, c) holds are not the mma's canonical columns but dims
+//    64j + 16c + 4t + {0..3}: one 16-byte load per row feeds four k steps. q
+//    takes the same permutation, so the dot products are unchanged;
+//  - builds the V operand of the P.V mma from the codes in the same way: the
+//    accumulator rows of m tile mt = 4q + u stand for dims 64q + 4g + u
+//    (row g) and 64q + 32 + 4g + u (row g + 8), so that a lane reads 4
+//    contiguous codes per token row and pairs the tokens' bytes with byte
+//    permutes; o is written back through the same map. No shared-memory
+//    tile is written, which leaves room for a third pipeline stage;
+//  - keeps q in f16 as a high and a low part of q * sm_scale * log2 e *
+//    k_scale (q ~ hi + lo to ~2^-22 relative), and P as high and low parts,
+//    as the 16-bit tensor-core kernel does.
+// Work partition, walk, softmax and the partial-result layout (8 heads per
+// slot) are those of decode_mma_kernel.
+#pragma once
+
+#include <type_traits>
+
+#include "pd_decode_mma.cuh"
+
+namespace pd {
+
+template <int D>
+struct CfgF8 {
+    static constexpr int kStages = 3;
+    // 16-row tiles per stage: two at head_dim 128 (8 KB of K and V codes per
+    // stage), one at 256 (a tile is 4 KB already).
+    static constexpr int kSub = D <= 128 ? 2 : 1;
+    static constexpr int kTileRaw = kMmaRows * D;      // E4M3 bytes of one K (or V) tile
+    static constexpr int kQBytes = 8 * D * 2;
+    static constexpr int kVOff = kSub * kTileRaw;      // V tiles within a stage
+    static constexpr int kQOff = 2 * kSub * kTileRaw;  // q rows within a stage
+    static constexpr int kStageBytes = round_up(kQOff + kQBytes, 128);
+    static constexpr int kMetaOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kMetaOff + kStages * 16;
+    static constexpr int kWarpBytes = round_up(kBarOff + kStages * 8, 128);
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kJ = D / 64;  // 64-dim groups: one 16-byte load per row each
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256, 1)
+    decode_fp8_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap) {
+    static_assert(D == 128 || D == 256, "head_dim 128 or 256");
+    using C = CfgF8<D>;
+    using M = __half;  // mma operand type
+    constexpr int kS = C::kStages, kKS = C::kKSteps;
+    constexpr float kShift = 7.f;  // f16 P: weights kept 2^7 larger, taken out of lse
+    constexpr float kTauM = 8.0f;
+    const float kNegInf = -__int_as_float(0x7f800000);
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int* s_indptr = reinterpret_cast<int*>(smem);
+    int* s_lpl = s_indptr + kTableMax + 1;
+    uint8_t* wsm = smem + a.table_bytes + wid * C::kWarpBytes;
+    int4* meta = reinterpret_cast<int4*>(wsm + C::kMetaOff);
+    const uint32_t wsm_u32 = smem_u32(wsm);
+    const uint32_t bar0 = wsm_u32 + C::kBarOff;
+
+    const long long gwarp = (long long)blockIdx.x * nwarps + wid;
+    const long long p0 = gwarp * a.pos_per_warp;
+    const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
+    Walk<false> walk(a, s_indptr, s_lpl, p0, pend, lane);
+    const int first_page = walk.prefetch_first();
+    const int GT = a.heads_per_tile;
+
+    walk.stage_table(s_indptr, s_lpl, [&] {
+        if (lane == 0) {
+            for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
+            fence_mbar_init();
+        }
+        walk.template prefetch_first_slabs<false>(first_page, 2 * kS, size_t(D));
+    });
+    __syncthreads();  // the only block-wide barrier
+    launch_dependents();
+    if (p0 >= pend) return;
+    walk.build(p0, first_page);
+
+    const uint64_t policy = l2_evict_first_policy();
+    const size_t q_row_bytes = size_t(D) * sizeof(T);
+    // Emit the next one or two chunks into `slot`. A chunk without kSegEnd
+    // is always followed by one of the same segment (same request and kv
+    // head): a second chunk is taken only then, so a stage never spans two
+    // segments.
+    auto produce = [&](int slot) {
+        Chunk c0, c1;
+        const bool have = walk.template next<kMmaRows>(&c0);
+        const bool two = (C::kSub == 2 && have && !(c0.flags & kSegEnd)) ? walk.template next<kMmaRows>(&c1) : false;
+        if (lane != 0) return;
+        const uint32_t bar = bar0 + 8 * slot;
+        const uint32_t st = wsm_u32 + slot * C::kStageBytes;
+        if (!have) {
+            meta[slot] = make_int4(0, kEndOfWork, 0, 0);
+            mbar_arrive(bar);
+            return;
+        }
+        const int r1 = two ? c1.rows : 0;
+        const int flags = two ? ((c0.flags & ~kSegEnd) | (c1.flags & kSegEnd)) : c0.flags;
+        meta[slot] = make_int4(c0.rows | (r1 << 16), flags, c0.qrow, c0.seg);
+        const uint32_t b0 = uint32_t(c0.rows) * uint32_t(D), b1 = uint32_t(r1) * uint32_t(D);
+        const uint32_t q_bytes = (flags & kSegStart) ? uint32_t(GT * q_row_bytes) : 0u;
+        const uint32_t total = 2 * (b0 + b1) + q_bytes;
+        if (total == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, total);
+        if (b0) {
+            const size_t off = kv_row<false>(a, c0.slab, c0.kh, c0.row0) * size_t(D);
+            bulk_g2s(st, static_cast<const uint8_t*>(a.k) + off, b0, bar, policy);
+            bulk_g2s(st + C::kVOff, static_cast<const uint8_t*>(a.v) + off, b0, bar, policy);
+        }
+        if (b1) {
+            const size_t off = kv_row<false>(a, c1.slab, c1.kh, c1.row0) * size_t(D);
+            bulk_g2s(st + C::kTileRaw, static_cast<const uint8_t*>(a.k) + off, b1, bar, policy);
+            bulk_g2s(st + C::kVOff + C::kTileRaw, static_cast<const uint8_t*>(a.v) + off, b1, bar, policy);
+        }
+        if (q_bytes)
+            bulk_g2s(st + C::kQOff, static_cast<const uint8_t*>(a.q) + size_t(c0.qrow) * q_row_bytes, q_bytes, bar);
+    };
+
+    // ---- consumer state: lane (g, c) owns tokens g, g+8 of each tile and heads 2c, 2c+1
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t qh[kKS][2], ql[kKS][2];  // score-mma B fragments (permuted dims), high and low f16 parts
+    float acc[kKS][4];  // P.V accumulators: o^T[v_dim(mt, 0 / 1)][head 2c (+1)]
+    // The dim that accumulator row g (hi = 0) or g + 8 (hi = 1) of m tile mt stands for.
+    auto v_dim = [&](int mt, int hi) { return 64 * (mt >> 2) + 32 * hi + 4 * g + (mt & 3); };
+    float m0, m1, l0, l1;
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int mt = 0; mt < kKS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        m0 = m1 = kNegInf;
+        l0 = l1 = 0.f;
+    };
+    reset_state();
+#pragma unroll
+    for (int kk = 0; kk < kKS; ++kk) qh[kk][0] = qh[kk][1] = ql[kk][0] = ql[kk][1] = 0u;
+
+    auto finalize = [&](int4 m) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, off);
+            l1 += __shfl_xor_sync(kFull, l1, off);
+        }
+        const int qrow = m.z;
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+        const float vsc = __ldg(a.v_scale + (qrow % a.num_qo_heads) / a.group);  // V scale, applied once
+        const float inv0 = l0 > 0.f ? vsc / l0 : 0.f, inv1 = l1 > 0.f ? vsc / l1 : 0.f;
+        const float lse0 = l0 > 0.f ? m0 - kShift + log2f(l0) : kNegInf;
+        const float lse1 = l1 > 0.f ? m1 - kShift + log2f(l1) : kNegInf;
+        if (m.y & kSegComplete) {
+            T* o0 = static_cast<T*>(a.o) + (size_t(qrow) + h0) * D;
+            T* o1 = o0 + D;
+#pragma unroll
+            for (int mt = 0; mt < kKS; ++mt) {
+                const int d = v_dim(mt, 0), d8 = v_dim(mt, 1);
+                if (h0 < GT) {
+                    o0[d] = T(acc[mt][0] * inv0);
+                    o0[d8] = T(acc[mt][2] * inv0);
+                }
+                if (h1 < GT) {
+                    o1[d] = T(acc[mt][1] * inv1);
+                    o1[d8] = T(acc[mt][3] * inv1);
+                }
+            }
+            if (g == 0 && a.lse != nullptr) {
+                if (h0 < GT) a.lse[size_t(qrow) + h0] = lse0 == kNegInf ? kNegInf : lse0 * kLn2;
+                if (h1 < GT) a.lse[size_t(qrow) + h1] = lse1 == kNegInf ? kNegInf : lse1 * kLn2;
+            }
+        } else {
+            const long long slot = gwarp + m.w;
+            float* p0r = a.part_o + (size_t(slot) * 8 + h0) * D;
+            float* p1r = p0r + D;
+#pragma unroll
+            for (int mt = 0; mt < kKS; ++mt) {
+                const int d = v_dim(mt, 0), d8 = v_dim(mt, 1);
+                if (h0 < GT) {
+                    p0r[d] = acc[mt][0] * inv0;
+                    p0r[d8] = acc[mt][2] * inv0;
+                }
+                if (h1 < GT) {
+                    p1r[d] = acc[mt][1] * inv1;
+                    p1r[d8] = acc[mt][3] * inv1;
+                }
+            }
+            if (g == 0) {
+                if (h0 < GT) a.part_lse[size_t(slot) * 8 + h0] = lse0;
+                if (h1 < GT) a.part_lse[size_t(slot) * 8 + h1] = lse1;
+            }
+        }
+        reset_state();
+    };
+
+    auto consume = [&](int slot, int4 m) {
+        const uint8_t* stp = wsm + slot * C::kStageBytes;
+        const int rows[2] = {m.x & 0xffff, m.x >> 16};
+        if (m.y & kSegStart) {
+            // q of head g at the permuted dims of k step kk = 4j + t:
+            // 64j + 16c + 4t + {0, 1} (first register), + {2, 3} (second).
+            const float qs = a.q_scale * __ldg(a.k_scale + (m.z % a.num_qo_heads) / a.group);
+            const uint8_t* qb = stp + C::kQOff + g * D * 2;
+#pragma unroll
+            for (int kk = 0; kk < kKS; ++kk) {
+                const int d0 = 64 * (kk >> 2) + 16 * c + 4 * (kk & 3);
+                uint2 w = make_uint2(0u, 0u);
+                if (g < GT) w = *reinterpret_cast<const uint2*>(qb + d0 * 2);
+                const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float2 v = unpack_pair<T>(ww[hf]);
+                    v.x *= qs;
+                    v.y *= qs;
+                    qh[kk][hf] = pack_pair<M>(v.x, v.y);
+                    const float2 r = unpack_pair<M>(qh[kk][hf]);
+                    ql[kk][hf] = pack_pair<M>(v.x - r.x, v.y - r.y);
+                }
+            }
+        }
+        // scores of both tiles: S_s[16 tokens][8 heads], K fragments from the codes
+        float sc[2][4];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            sc[s][0] = sc[s][1] = sc[s][2] = sc[s][3] = 0.f;
+            if (s >= C::kSub || rows[s] == 0) continue;
+            const uint8_t* kr = stp + s * C::kTileRaw + 16 * c;
+#pragma unroll
+            for (int j = 0; j < C::kJ; ++j) {
+                const uint4 wa = *reinterpret_cast<const uint4*>(kr + g * D + 64 * j);
+                const uint4 wb = *reinterpret_cast<const uint4*>(kr + (g + 8) * D + 64 * j);
+                const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int kk = 4 * j + t;
+                    const uint32_t af[4] = {e4m3x2_to_f16x2(xa[t]), e4m3x2_to_f16x2(xb[t]),
+                                            e4m3x2_to_f16x2(xa[t] >> 16), e4m3x2_to_f16x2(xb[t] >> 16)};
+                    mma_16816<M>(sc[s], af, qh[kk][0], qh[kk][1]);
+                    mma_16816<M>(sc[s], af, ql[kk][0], ql[kk][1]);
+                }
+            }
+        }
+        // softmax over the 32 tokens; x[s][i]: tile s, token g (i = 0, 1) or
+        // g + 8 (i = 2, 3), head 2c (i even) or 2c + 1 (i odd)
+        float x[2][4];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            x[s][0] = g < rows[s] ? sc[s][0] : kNegInf;
+            x[s][1] = g < rows[s] ? sc[s][1] : kNegInf;
+            x[s][2] = g + 8 < rows[s] ? sc[s][2] : kNegInf;
+            x[s][3] = g + 8 < rows[s] ? sc[s][3] : kNegInf;
+        }
+        const float c0l = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+        const float c1l = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+        if (__any_sync(kFull, c0l > m0 + kTauM || c1l > m1 + kTauM)) {
+            float c0 = c0l, c1 = c1l;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                c0 = fmaxf(c0, __shfl_xor_sync(kFull, c0, off));
+                c1 = fmaxf(c1, __shfl_xor_sync(kFull, c1, off));
+            }
+            const float n0 = fmaxf(m0, c0), n1 = fmaxf(m1, c1);
+            const float al0 = n0 == kNegInf ? 1.f : ex2(m0 - n0), al1 = n1 == kNegInf ? 1.f : ex2(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < kKS; ++mt) {
+                acc[mt][0] *= al0;
+                acc[mt][2] *= al0;
+                acc[mt][1] *= al1;
+                acc[mt][3] *= al1;
+            }
+        }
+        uint32_t bh[2][2], bl[2][2];  // P.V B fragments of each tile, high and low parts
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const float p0 = x[s][0] == kNegInf ? 0.f : ex2(x[s][0] - m0 + kShift);
+            const float p1 = x[s][1] == kNegInf ? 0.f : ex2(x[s][1] - m1 + kShift);
+            const float p2 = x[s][2] == kNegInf ? 0.f : ex2(x[s][2] - m0 + kShift);
+            const float p3 = x[s][3] == kNegInf ? 0.f : ex2(x[s][3] - m1 + kShift);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            const uint32_t h01 = pack_pair<M>(p0, p1), h23 = pack_pair<M>(p2, p3);
+            const float2 r01 = unpack_pair<M>(h01), r23 = unpack_pair<M>(h23);
+            const uint32_t l01 = pack_pair<M>(p0 - r01.x, p1 - r01.y), l23 = pack_pair<M>(p2 - r23.x, p3 - r23.y);
+            bh[s][0] = movm_trans(h01);
+            bh[s][1] = movm_trans(h23);
+            bl[s][0] = movm_trans(l01);
+            bl[s][1] = movm_trans(l23);
+        }
+        // O^T[head_dim][8 heads] += V_s^T[head_dim][16 tokens] P_s[16 tokens][8 heads]. Lane (g, c)
+        // holds tokens 2c, 2c+1 (first register pair) and 2c+8, 2c+9 (second)
+        // of the A fragment: it loads, per token and 64-dim group q, the codes
+        // of dims 64q + 4g + {0..3} and 64q + 32 + 4g + {0..3} (zero for rows
+        // past the valid length, whose zero weights must not meet a NaN code)
+        // and pairs the two tokens' bytes u for m tile 4q + u.
+#pragma unroll
+        for (int s = 0; s < C::kSub; ++s) {
+            if (rows[s] == 0) continue;
+            const uint8_t* vr = stp + C::kVOff + s * C::kTileRaw + 4 * g;
+            const int t0 = 2 * c;
+#pragma unroll
+            for (int q = 0; q < C::kJ; ++q) {
+                uint32_t w[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tk = t0 + (i & 1) + 8 * (i >> 1);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        w[i][h] = tk < rows[s] ? *reinterpret_cast<const uint32_t*>(vr + tk * D + 64 * q + 32 * h) : 0u;
+                }
+                // pr[pair][h][half]: bytes u of tokens (t0, t0+1) (pair 0) or
+                // (t0+8, t0+9) (pair 1), u = 2 * half + (0 | 1 in the 16-bit halves)
+                uint32_t pr[2][2][2];
+#pragma unroll
+                for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        pr[pi][h][0] = __byte_perm(w[2 * pi][h], w[2 * pi + 1][h], 0x5140);
+                        pr[pi][h][1] = __byte_perm(w[2 * pi][h], w[2 * pi + 1][h], 0x7362);
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int mt = 4 * q + u, sh = 16 * (u & 1);
+                    const uint32_t af[4] = {e4m3x2_to_f16x2(pr[0][0][u >> 1] >> sh), e4m3x2_to_f16x2(pr[0][1][u >> 1] >> sh),
+                                            e4m3x2_to_f16x2(pr[1][0][u >> 1] >> sh), e4m3x2_to_f16x2(pr[1][1][u >> 1] >> sh)};
+                    mma_16816<M>(acc[mt], af, bh[s][0], bh[s][1]);
+                    mma_16816<M>(acc[mt], af, bl[s][0], bl[s][1]);
+                }
+            }
+        }
+        if (m.y & kSegEnd) finalize(m);
+    };
+
+#pragma unroll 1
+    for (int s = 0; s < kS; ++s) produce(s);
+#pragma unroll 1
+    for (int it = 0;; ++it) {
+        const int slot = it % kS;
+        const uint32_t parity = uint32_t(it / kS) & 1u;
+        if (!mbar_wait_bounded(bar0 + 8 * slot, parity)) {
+            if (lane == 0) atomicOr(a.flags, kFlagTimeout);
+            for (int s = 1; s < kS; ++s) {
+                const int it2 = it + s;
+                mbar_wait_bounded(bar0 + 8 * (it2 % kS), uint32_t(it2 / kS) & 1u);
+            }
+            break;
+        }
+        const int4 m = meta[slot];
+        if (m.y & kEndOfWork) break;
+        consume(slot, m);
+        __syncwarp();
+        produce(slot);
+    }
+}
+
+}  // namespace pd

@@ -212,6 +212,15 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float* f) {
     }
 }
 
+// Two E4M3 codes (the low 16 bits of w, first code in the low byte) to an
+// f16x2 word, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+    uint32_t out;
+    memcpy(&out, &r, 4);
+    return out;
+}
+
 template <typename T>
 struct Elt;
 

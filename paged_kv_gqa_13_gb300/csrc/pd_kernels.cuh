@@ -4,6 +4,7 @@
 #include <type_traits>
 
 #include "pd_decode.cuh"
+#include "pd_decode_fp8.cuh"
 #include "pd_decode_mma.cuh"
 #include "pd_merge.cuh"
 
@@ -17,7 +18,8 @@ struct KernelSet {
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
     int rows_per_stage;  // K (and V) rows one pipeline stage holds
-    int mma;             // 1: tensor-core kernel (K/V always through 128B-swizzled tensor maps)
+    int mma;             // 1: K/V copies through 128B-swizzled tensor maps (tensor-core kernel, 16-bit pools)
+    int part_heads;      // heads per partial-result slot: the group tile G, or 8 for the tensor-core kernel
     int smem_slack;      // extra dynamic shared memory for aligning the stages
 };
 
@@ -33,12 +35,14 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
             ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                 \
             ks->rows_per_stage = kMmaRows;                                              \
             ks->mma = 1;                                                                \
+            ks->part_heads = 8;                                                         \
             ks->smem_slack = 1024;                                                      \
         } else {                                                                        \
             ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);     \
             ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
             ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                   \
             ks->mma = 0;                                                                \
+            ks->part_heads = GG;                                                        \
             ks->smem_slack = 0;                                                         \
         }                                                                               \
         return true;                                                                    \
@@ -72,23 +76,33 @@ bool lookup_variant_t(int D, int G, const void** fn) {
     return false;
 }
 
-// The decode kernel for E4M3 pools with q / o of type T (16-bit): the
-// CUDA-core decode at every group size, with its own stage geometry. The
-// merge kernels are those of T (from lookup_kernels_t), left untouched here.
+// The decode kernel for E4M3 pools with q / o of type T (16-bit). Tiles of 4
+// or more q heads at head_dim 128 / 256 go to the tensor-core kernel (the
+// CUDA cores would be issue-bound there: an E4M3 byte is a whole element);
+// the rest to the CUDA-core kernel. The merge kernels are those of T (from
+// lookup_kernels_t), left untouched here.
 template <typename T>
 bool lookup_fp8_t(int D, int G, KernelSet* ks) {
     static_assert(sizeof(T) == 2, "E4M3 pools take 16-bit q / o");
-#define PD_CASE(DD, GG)                                                                 \
-    if (D == DD && G == GG) {                                                           \
-        using C = Cfg<T, DD, GG, 1>;                                                    \
-        ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVarFp8>);  \
-        ks->warp_bytes = C::kWarpBytes;                                                 \
-        ks->rows_per_stage = C::kRC;                                                    \
-        ks->mma = 0;                                                                    \
-        ks->smem_slack = 0;                                                             \
-        ks->variant[0] = ks->decode;                                                    \
-        ks->variant[1] = ks->variant[2] = ks->variant[3] = nullptr;                     \
-        return true;                                                                    \
+#define PD_CASE(DD, GG)                                                                      \
+    if (D == DD && G == GG) {                                                                \
+        if constexpr (DD >= 128 && GG >= 4) {                                                \
+            ks->decode = reinterpret_cast<const void*>(decode_fp8_mma_kernel<T, DD>);        \
+            ks->warp_bytes = CfgF8<DD>::kWarpBytes;                                          \
+            ks->rows_per_stage = kMmaRows;                                                   \
+            ks->part_heads = 8;                                                              \
+            ks->smem_slack = 0;                                                              \
+        } else {                                                                             \
+            ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVarFp8>);   \
+            ks->warp_bytes = Cfg<T, DD, GG, 1>::kWarpBytes;                                  \
+            ks->rows_per_stage = Cfg<T, DD, GG, 1>::kRC;                                     \
+            ks->part_heads = GG;                                                             \
+            ks->smem_slack = 0;                                                              \
+        }                                                                                    \
+        ks->mma = 0;                                                                         \
+        ks->variant[0] = ks->decode;                                                         \
+        ks->variant[1] = ks->variant[2] = ks->variant[3] = nullptr;                          \
+        return true;                                                                         \
     }
     PD_CASE(64, 1) PD_CASE(64, 2) PD_CASE(64, 4) PD_CASE(64, 8)
     PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)
