@@ -201,7 +201,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     if (st != PD_OK) return st;
     p->table_bytes = pd::table_bytes_for(!contiguous && batch <= pd::kTableMax);
     p->nwarps = (di.max_smem - p->table_bytes - p->ks.smem_slack) / p->ks.warp_bytes;
-    if (p->nwarps > 8) p->nwarps = 8;
+    if (p->nwarps > p->ks.max_warps) p->nwarps = p->ks.max_warps;
     if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
     p->smem = size_t(p->ks.smem_slack) + size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
     // The variants this plan may launch (NHD only on the contiguous cache) all

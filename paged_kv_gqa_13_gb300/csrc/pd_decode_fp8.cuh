@@ -37,7 +37,12 @@ namespace pd {
 
 template <int D>
 struct CfgF8 {
-    static constexpr int kStages = 3;
+    // Two stages and up to 11 warps per block at head_dim 128: the step's
+    // instruction stream is latency-bound, so warps (not stages) are what
+    // hides it; 11 warps x 2 stages keep more bytes in flight than 7 x 3.
+    // At 256 the registers of 11 warps would not hold the accumulators: 8.
+    static constexpr int kStages = 2;
+    static constexpr int kMaxWarps = D <= 128 ? 11 : 8;
     // 16-row tiles per stage: two at head_dim 128 (8 KB of K and V codes per
     // stage), one at 256 (a tile is 4 KB already).
     static constexpr int kSub = D <= 128 ? 2 : 1;
@@ -54,7 +59,7 @@ struct CfgF8 {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     decode_fp8_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap) {
     static_assert(D == 128 || D == 256, "head_dim 128 or 256");
     using C = CfgF8<D>;
@@ -234,28 +239,42 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-        // scores of both tiles: S_s[16 tokens][8 heads], K fragments from the codes
-        float sc[2][4];
+        // scores of both tiles: S_s[16 tokens][8 heads], K fragments from the
+        // codes. The high and low q parts go to separate accumulators, and the
+        // k steps of both tiles interleave: four independent mma chains.
+        float sc[2][4], sl[2][4];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            sc[s][0] = sc[s][1] = sc[s][2] = sc[s][3] = 0.f;
-            if (s >= C::kSub || rows[s] == 0) continue;
-            const uint8_t* kr = stp + s * C::kTileRaw + 16 * c;
+        for (int s = 0; s < 2; ++s)
 #pragma unroll
-            for (int j = 0; j < C::kJ; ++j) {
-                const uint4 wa = *reinterpret_cast<const uint4*>(kr + g * D + 64 * j);
-                const uint4 wb = *reinterpret_cast<const uint4*>(kr + (g + 8) * D + 64 * j);
-                const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
+            for (int i = 0; i < 4; ++i) sc[s][i] = sl[s][i] = 0.f;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int kk = 4 * j + t;
-                    const uint32_t af[4] = {e4m3x2_to_f16x2(xa[t]), e4m3x2_to_f16x2(xb[t]),
-                                            e4m3x2_to_f16x2(xa[t] >> 16), e4m3x2_to_f16x2(xb[t] >> 16)};
+        for (int j = 0; j < C::kJ; ++j) {
+            uint32_t xa[2][4], xb[2][4];
+#pragma unroll
+            for (int s = 0; s < C::kSub; ++s) {
+                const uint8_t* kr = stp + s * C::kTileRaw + 16 * c + 64 * j;
+                const uint4 wa = *reinterpret_cast<const uint4*>(kr + g * D);
+                const uint4 wb = *reinterpret_cast<const uint4*>(kr + (g + 8) * D);
+                xa[s][0] = wa.x, xa[s][1] = wa.y, xa[s][2] = wa.z, xa[s][3] = wa.w;
+                xb[s][0] = wb.x, xb[s][1] = wb.y, xb[s][2] = wb.z, xb[s][3] = wb.w;
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int kk = 4 * j + t;
+#pragma unroll
+                for (int s = 0; s < C::kSub; ++s) {
+                    if (rows[s] == 0) continue;
+                    const uint32_t af[4] = {e4m3x2_to_f16x2(xa[s][t]), e4m3x2_to_f16x2(xb[s][t]),
+                                            e4m3x2_to_f16x2(xa[s][t] >> 16), e4m3x2_to_f16x2(xb[s][t] >> 16)};
                     mma_16816<M>(sc[s], af, qh[kk][0], qh[kk][1]);
-                    mma_16816<M>(sc[s], af, ql[kk][0], ql[kk][1]);
+                    mma_16816<M>(sl[s], af, ql[kk][0], ql[kk][1]);
                 }
             }
         }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[s][i] += sl[s][i];
         // softmax over the 32 tokens; x[s][i]: tile s, token g (i = 0, 1) or
         // g + 8 (i = 2, 3), head 2c (i even) or 2c + 1 (i odd)
         float x[2][4];

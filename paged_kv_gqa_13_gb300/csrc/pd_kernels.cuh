@@ -21,6 +21,7 @@ struct KernelSet {
     int mma;             // 1: K/V copies through 128B-swizzled tensor maps (tensor-core kernel, 16-bit pools)
     int part_heads;      // heads per partial-result slot: the group tile G, or 8 for the tensor-core kernel
     int smem_slack;      // extra dynamic shared memory for aligning the stages
+    int max_warps;       // warps per block the kernel is built for (its launch bound / 32)
 };
 
 template <typename T>
@@ -37,6 +38,7 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
             ks->mma = 1;                                                                \
             ks->part_heads = 8;                                                         \
             ks->smem_slack = 1024;                                                      \
+            ks->max_warps = 8;                                                          \
         } else {                                                                        \
             ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);     \
             ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
@@ -44,6 +46,7 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
             ks->mma = 0;                                                                \
             ks->part_heads = GG;                                                        \
             ks->smem_slack = 0;                                                         \
+            ks->max_warps = 8;                                                          \
         }                                                                               \
         return true;                                                                    \
     }
@@ -92,12 +95,14 @@ bool lookup_fp8_t(int D, int G, KernelSet* ks) {
             ks->rows_per_stage = kMmaRows;                                                   \
             ks->part_heads = 8;                                                              \
             ks->smem_slack = 0;                                                              \
+            ks->max_warps = CfgF8<DD>::kMaxWarps;                                            \
         } else {                                                                             \
             ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVarFp8>);   \
             ks->warp_bytes = Cfg<T, DD, GG, 1>::kWarpBytes;                                  \
             ks->rows_per_stage = Cfg<T, DD, GG, 1>::kRC;                                     \
             ks->part_heads = GG;                                                             \
             ks->smem_slack = 0;                                                              \
+            ks->max_warps = 8;                                                               \
         }                                                                                    \
         ks->mma = 0;                                                                         \
         ks->variant[0] = ks->decode;                                                         \
