@@ -37,7 +37,8 @@ UNIT = "TB/s"
 DEFAULT_CONFIG = "llama3_8b"
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["paged_kv_gqa_13_gb300/csrc/" + f for f in
-                  ("pd_device.cuh", "pd_walk.cuh", "pd_decode.cuh", "pd_decode_mma.cuh", "pd_merge.cuh")]
+                  ("pd_device.cuh", "pd_walk.cuh", "pd_decode.cuh", "pd_decode_mma.cuh", "pd_decode_fp8.cuh",
+                   "pd_merge.cuh")]
 
 
 def kernel_sha() -> str:
@@ -146,13 +147,13 @@ def load_workload(name: str, rank: int = 0):
 
 def decode_kernel_name(w, mode: str = "paged") -> str:
     """The decode kernel the library picks for this workload (tensor cores for
-    16-bit tiles of 5..8 q heads per kv head, CUDA cores otherwise and for
-    E4M3 pools)."""
-    if mode == "paged_fp8":
-        return "decode_kernel"
+    16-bit tiles of 5..8 q heads per kv head, CUDA cores otherwise; for E4M3
+    pools, tensor cores for tiles of 4..8 at head_dim 128 / 256)."""
     g = w.group
     tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
     per_tile = g // tiles
+    if mode == "paged_fp8":
+        return "decode_fp8_mma_kernel" if (w.head_dim >= 128 and per_tile > 2) else "decode_kernel"
     return "decode_mma_kernel" if (w.dtype != "f32" and per_tile > 4) else "decode_kernel"
 
 
