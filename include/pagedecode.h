@@ -319,6 +319,18 @@ pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream);
  * event records per kernel; it is off by default.
  */
 pd_status pd_profile_enable(int enable);
+
+/*
+ * Test-only failure injection for the bounded waits. While extra_bytes is
+ * nonzero (a multiple of 16, at most 1 MiB), every decode call's first warp
+ * waits, for its first pipeline stage, for extra_bytes more than its copies
+ * deliver. Its wait gives up after its limit (2 s), sets
+ * PD_FLAG_WAIT_TIMEOUT in the status word, lets its other stages' copies
+ * land, and returns; the outputs of the requests it held are then undefined,
+ * and the GPU context stays usable. 0 (the default) turns it off.
+ * Process-wide; not for use alongside other decode calls.
+ */
+pd_status pd_test_inject_wait_timeout(int extra_bytes);
 pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge_ms,
                           int* merge_launches, double* append_ms, int* append_launches);
 

@@ -47,6 +47,7 @@ _SIGS = {
     "pd_read_device_flags": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "pd_copy_bytes": (_I, [_P, _P, _S, _P]),
     "pd_profile_enable": (_I, [_I]),
+    "pd_test_inject_wait_timeout": (_I, [_I]),
     "pd_profile_read": (_I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
@@ -323,3 +324,8 @@ def pd_paged_append_fp8(k_new, v_new, k_scale, v_scale, k_data, v_data, indices,
         _ptr(indices) if indices.numel() else None, _ptr(indptr), _ptr(last_page_len), batch, num_kv_heads,
         head_dim, page_size, num_total_pages, indices.numel(), _dtype_code(k_new), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+
+
+def pd_test_inject_wait_timeout(extra_bytes: int) -> None:
+    """Test-only: make each decode's first warp wait for bytes that never arrive (0 turns it off)."""
+    _check(_lib.pd_test_inject_wait_timeout(int(extra_bytes)))

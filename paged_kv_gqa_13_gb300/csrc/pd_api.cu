@@ -1,5 +1,6 @@
 // The C ABI of pagedecode: argument checks, planning of the work partition,
 // kernel launches, the paged append and copy kernels, profiling hooks.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -312,10 +313,14 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 
 // ---------------------------------------------------------------- decode launch
 
+// Test-only: extra bytes warp 0's first pipeline stage waits for (0: off).
+std::atomic<int> g_inject_extra_tx{0};
+
 // nhd: the contiguous cache is token-major, [slabs, slab_rows, Hk, D].
 pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, bool nhd,
                         cudaStream_t stream) {
     const int variant = (a.k_new != nullptr ? pd::kVarFused : 0) | (nhd ? pd::kVarNhd : 0);
+    a.test_extra_tx = g_inject_extra_tx.load(std::memory_order_relaxed);
     // Every decode kernel takes two tensor maps; they are read by the
     // tensor-core kernel and by the CUDA-core kernel's NHD variants.
     CUtensorMap maps[2];
@@ -915,6 +920,13 @@ pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream) 
         static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+    return ok();
+}
+
+pd_status pd_test_inject_wait_timeout(int extra_bytes) {
+    if (extra_bytes < 0 || extra_bytes > (1 << 20) || extra_bytes % 16 != 0)
+        return fail(PD_ERR_INVALID, "extra_bytes must be a multiple of 16 in [0, 1 MiB]");
+    g_inject_extra_tx.store(extra_bytes, std::memory_order_relaxed);
     return ok();
 }
 

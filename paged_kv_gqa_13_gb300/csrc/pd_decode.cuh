@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(256, 1)
     const size_t row_bytes = size_t(C::kRowBytes);       // q
     const size_t kv_row_bytes = size_t(C::kKvRowBytes);  // K, V
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
-    auto produce = [&](int slot) {
+    auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
         const bool have = walk.template next<kRC>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar);
             return;
         }
-        mbar_arrive_expect_tx(bar, total);
+        mbar_arrive_expect_tx(bar, total + extra_tx);
         if (kv_bytes) {
             if constexpr (kNhd) {
                 tma_load_4d(smem_u32(st), &tmk, 0, ck.kh, ck.row0, ck.slab, bar, policy);
@@ -398,8 +398,10 @@ __global__ void __launch_bounds__(256, 1)
     };
 
     // ---- pipeline
+    // a.test_extra_tx (test-only, normally 0): warp 0's first stage expects
+    // bytes that never arrive, so that its bounded wait runs out.
 #pragma unroll 1
-    for (int s = 0; s < kStages; ++s) produce(s);
+    for (int s = 0; s < kStages; ++s) produce(s, (s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u);
 #pragma unroll 1
     for (int it = 0;; ++it) {
         const int slot = it % kStages;
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(256, 1)
         if (m.y & kEndOfWork) break;
         consume(slot, m);
         __syncwarp();
-        produce(slot);
+        produce(slot, 0u);
     }
 }
 

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     // is always followed by one of the same segment (same request and kv
     // head): a second chunk is taken only then, so a stage never spans two
     // segments.
-    auto produce = [&](int slot) {
+    auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk c0, c1;
         const bool have = walk.template next<kMmaRows>(&c0);
         const bool two = (C::kSub == 2 && have && !(c0.flags & kSegEnd)) ? walk.template next<kMmaRows>(&c1) : false;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             mbar_arrive(bar);
             return;
         }
-        mbar_arrive_expect_tx(bar, total);
+        mbar_arrive_expect_tx(bar, total + extra_tx);
         if (b0) {
             const size_t off = kv_row<false>(a, c0.slab, c0.kh, c0.row0) * size_t(D);
             bulk_g2s(st, static_cast<const uint8_t*>(a.k) + off, b0, bar, policy);
@@ -369,8 +369,10 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         if (m.y & kSegEnd) finalize(m);
     };
 
+    // a.test_extra_tx (test-only, normally 0): warp 0's first stage expects
+    // bytes that never arrive, so that its bounded wait runs out.
 #pragma unroll 1
-    for (int s = 0; s < kS; ++s) produce(s);
+    for (int s = 0; s < kS; ++s) produce(s, (s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u);
 #pragma unroll 1
     for (int it = 0;; ++it) {
         const int slot = it % kS;
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         if (m.y & kEndOfWork) break;
         consume(slot, m);
         __syncwarp();
-        produce(slot);
+        produce(slot, 0u);
     }
 }
 

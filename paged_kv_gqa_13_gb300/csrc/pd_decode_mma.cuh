@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256, 1)
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(D) * sizeof(T);
-    auto produce = [&](int slot) {
+    auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
         const bool have = walk.template next<kMmaRows>(&ck);
         const uint32_t bar = bar0 + 8 * slot;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar);
             return;
         }
-        mbar_arrive_expect_tx(bar, total);
+        mbar_arrive_expect_tx(bar, total + extra_tx);
         if (kv_bytes) {
             const int c1 = kNhd ? ck.kh : ck.row0, c2 = kNhd ? ck.row0 : ck.kh;
 #pragma unroll
@@ -312,8 +312,10 @@ __global__ void __launch_bounds__(256, 1)
         if (m.y & kSegEnd) finalize(m);
     };
 
+    // a.test_extra_tx (test-only, normally 0): warp 0's first stage expects
+    // bytes that never arrive, so that its bounded wait runs out.
 #pragma unroll 1
-    for (int s = 0; s < kS; ++s) produce(s);
+    for (int s = 0; s < kS; ++s) produce(s, (s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u);
 #pragma unroll 1
     for (int it = 0;; ++it) {
         const int slot = it % kS;
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(256, 1)
         if (m.y & kEndOfWork) break;
         consume(slot, m);
         __syncwarp();
-        produce(slot);
+        produce(slot, 0u);
     }
 }
 

@@ -396,6 +396,7 @@ struct DecodeArgs {
     // FP8 pools (null otherwise): element value = E4M3 code value * scale[kv head].
     const float* k_scale;
     const float* v_scale;
+    int test_extra_tx;  // test-only wait-timeout injection (pd_test_inject_wait_timeout); normally 0
 };
 
 struct MergeArgs {
