@@ -24,7 +24,10 @@
 //    tile is written, which leaves room for a third pipeline stage;
 //  - keeps q in f16 as a high and a low part of q * sm_scale * log2 e *
 //    k_scale (q ~ hi + lo to ~2^-22 relative), and P as high and low parts,
-//    as the 16-bit tensor-core kernel does.
+//    as the 16-bit tensor-core kernel does. q is not staged with the pages:
+//    the producer pulls a segment's q rows into L2 with its first stage, and
+//    the consumer loads its fragments from there, which keeps a warp's shared
+//    memory to its two stages of codes.
 // Work partition, walk, softmax and the partial-result layout (8 heads per
 // slot) are those of decode_mma_kernel.
 #pragma once
@@ -37,20 +40,20 @@ namespace pd {
 
 template <int D>
 struct CfgF8 {
-    // Two stages and up to 11 warps per block at head_dim 128: the step's
+    // Two stages and up to 12 warps per block at head_dim 128: the step's
     // instruction stream is latency-bound, so warps (not stages) are what
-    // hides it; 11 warps x 2 stages keep more bytes in flight than 7 x 3.
-    // At 256 the registers of 11 warps would not hold the accumulators: 8.
+    // hides it; 12 warps x 2 stages keep more bytes in flight than 7 x 3.
+    // At 256 the registers of 12 warps would not hold the accumulators: 8.
     static constexpr int kStages = 2;
-    static constexpr int kMaxWarps = D <= 128 ? 11 : 8;
+    static constexpr int kMaxWarps = D <= 128 ? 12 : 8;
     // 16-row tiles per stage: two at head_dim 128 (8 KB of K and V codes per
     // stage), one at 256 (a tile is 4 KB already).
     static constexpr int kSub = D <= 128 ? 2 : 1;
     static constexpr int kTileRaw = kMmaRows * D;      // E4M3 bytes of one K (or V) tile
-    static constexpr int kQBytes = 8 * D * 2;
+
     static constexpr int kVOff = kSub * kTileRaw;      // V tiles within a stage
-    static constexpr int kQOff = 2 * kSub * kTileRaw;  // q rows within a stage
-    static constexpr int kStageBytes = round_up(kQOff + kQBytes, 128);
+    // q is not staged: it is read at a segment start, from L2 (see produce)
+    static constexpr int kStageBytes = round_up(2 * kSub * kTileRaw, 128);
     static constexpr int kMetaOff = kStages * kStageBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 16;
     static constexpr int kWarpBytes = round_up(kBarOff + kStages * 8, 128);
@@ -121,8 +124,12 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         const int flags = two ? ((c0.flags & ~kSegEnd) | (c1.flags & kSegEnd)) : c0.flags;
         meta[slot] = make_int4(c0.rows | (r1 << 16), flags, c0.qrow, c0.seg);
         const uint32_t b0 = uint32_t(c0.rows) * uint32_t(D), b1 = uint32_t(r1) * uint32_t(D);
-        const uint32_t q_bytes = (flags & kSegStart) ? uint32_t(GT * q_row_bytes) : 0u;
-        const uint32_t total = 2 * (b0 + b1) + q_bytes;
+        // A segment's q rows are pulled into L2 with its first stage; the
+        // consumer reads them from there when it reaches that stage.
+        if (flags & kSegStart)
+            bulk_prefetch_l2(static_cast<const uint8_t*>(a.q) + size_t(c0.qrow) * q_row_bytes,
+                             uint32_t(GT * q_row_bytes));
+        const uint32_t total = 2 * (b0 + b1);
         if (total == 0) {
             mbar_arrive(bar);
             return;
@@ -138,8 +145,6 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             bulk_g2s(st + C::kTileRaw, static_cast<const uint8_t*>(a.k) + off, b1, bar, policy);
             bulk_g2s(st + C::kVOff + C::kTileRaw, static_cast<const uint8_t*>(a.v) + off, b1, bar, policy);
         }
-        if (q_bytes)
-            bulk_g2s(st + C::kQOff, static_cast<const uint8_t*>(a.q) + size_t(c0.qrow) * q_row_bytes, q_bytes, bar);
     };
 
     // ---- consumer state: lane (g, c) owns tokens g, g+8 of each tile and heads 2c, 2c+1
@@ -221,12 +226,12 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             // q of head g at the permuted dims of k step kk = 4j + t:
             // 64j + 16c + 4t + {0, 1} (first register), + {2, 3} (second).
             const float qs = a.q_scale * __ldg(a.k_scale + (m.z % a.num_qo_heads) / a.group);
-            const uint8_t* qb = stp + C::kQOff + g * D * 2;
+            const uint8_t* qb = static_cast<const uint8_t*>(a.q) + (size_t(m.z) + g) * q_row_bytes;
 #pragma unroll
             for (int kk = 0; kk < kKS; ++kk) {
                 const int d0 = 64 * (kk >> 2) + 16 * c + 4 * (kk & 3);
                 uint2 w = make_uint2(0u, 0u);
-                if (g < GT) w = *reinterpret_cast<const uint2*>(qb + d0 * 2);
+                if (g < GT) w = __ldg(reinterpret_cast<const uint2*>(qb + d0 * 2));
                 const uint32_t ww[2] = {w.x, w.y};
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
