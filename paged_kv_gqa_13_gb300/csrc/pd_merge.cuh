@@ -9,11 +9,13 @@ namespace pd {
 // Weighted sum of partial rows, parts taken in index order: lane c of each
 // group of 32 parts computes its part's weight 2^(lse_c - L); the weights are
 // broadcast with shuffles and every lane accumulates its kPer columns.
-template <int kPer, class LseAt, class RowAt>
+// kFastMax bounds the parts whose rows are all loaded before any is used, and
+// kGroup the rows in flight beyond that: the register budget of the caller.
+template <int kPer, int kFastMax = 16, int kGroup = 8, class LseAt, class RowAt>
 __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_at, float* acc) {
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;
-    constexpr int kFast = (64 / kPer) < 16 ? (64 / kPer) : 16;  // parts kept in registers
+    constexpr int kFast = (64 / kPer) < kFastMax ? (64 / kPer) : kFastMax;  // parts kept in registers
     if (parts <= kFast) {
         // One round trip: every part's lse and row are requested before any
         // weight is known.
@@ -57,10 +59,10 @@ __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_a
     for (int base = 0; base < parts; base += 32) {
         const int n = min(32, parts - base);
         const float w_mine = (lane < n) ? ex2(lse_at(base + lane) - L) : 0.f;
-        for (int j0 = 0; j0 < n; j0 += 8) {
-            float rows[8][kPer];  // eight rows in flight before any is used
+        for (int j0 = 0; j0 < n; j0 += kGroup) {
+            float rows[kGroup][kPer];  // kGroup rows in flight before any is used
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kGroup; ++j) {
                 if (j0 + j < n) {
                     const float* po = row_at(base + j0 + j) + lane * kPer;
 #pragma unroll
@@ -72,7 +74,7 @@ __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_a
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kGroup; ++j) {
                 const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
                 if (j0 + j < n) {
 #pragma unroll
@@ -104,7 +106,11 @@ __device__ __forceinline__ void store_row(T* orow, const float* acc) {
 // not depend on the decode's output (the page table, empty requests) is done
 // before waiting for the decode grid.
 template <typename T, int D>
-__global__ void __launch_bounds__(128, 1) merge_partials_kernel(const MergeArgs a) {
+// Its grid follows the decode with one warp per (segment, head); registers
+// are held to 85 per thread (8 parts in registers and groups of 4 beyond, 4
+// and 2 at head_dim 256) so that 6 blocks fit per SM and the warps that remain
+// after the decode run in few waves.
+__global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs a) {
     constexpr int kPer = D / 32;  // elements per lane
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(128, 1) merge_partials_kernel(const MergeArgs 
         grid_dependency_wait();     // the decode kernel's partials are complete and visible
         const int parts = int(last - first + 1);
         const long long slot0 = (first + s) * a.G + h;  // slot of part c: (first + c + s) * G + h
-        L = merge_rows<kPer>(
+        L = merge_rows<kPer, (D <= 128 ? 8 : 4), (D <= 128 ? 4 : 2)>(
             parts, [&](int cp) { return a.part_lse[slot0 + (long long)cp * a.G]; },
             [&](int cp) { return a.part_o + size_t(slot0 + (long long)cp * a.G) * D; }, acc);
     }
