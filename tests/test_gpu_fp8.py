@@ -61,6 +61,9 @@ LENS = [0, 1, 15, 16, 17, 100, 3000, 33]
     ("f16", 24, 2, 128, 8),     # group 12: two head tiles, page 8
     ("bf16", 32, 8, 256, 16),   # group 4, D 256 (tensor cores)
     ("f16", 16, 8, 128, 16),    # group 2 (CUDA cores)
+    ("bf16", 32, 8, 128, 1),    # one-row pages: two one-row chunks per stage
+    ("f16", 64, 8, 128, 100),   # pages of 100 rows: 16-row chunks and a 4-row remainder
+    ("bf16", 32, 8, 64, 16),    # group 4 at D 64 (CUDA cores)
 ])
 def test_fp8_decode_matches_oracle(dtype, Hq, Hk, D, P):
     w = wl.make_paged(f"fp8_{dtype}_{Hq}_{Hk}_{D}", dtype, LENS, Hq, Hk, D, P, seed=300 + Hq + D + P)
