@@ -154,7 +154,7 @@ def decode_kernel_name(w, mode: str = "paged") -> str:
     per_tile = g // tiles
     if mode == "paged_fp8":
         return "decode_fp8_mma_kernel" if (w.head_dim >= 128 and per_tile > 2) else "decode_kernel"
-    return "decode_mma_kernel" if (w.dtype != "f32" and per_tile > 4) else "decode_kernel"
+    return "decode_mma_kernel" if (w.dtype != "f32" and per_tile >= 4) else "decode_kernel"
 
 
 def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:

@@ -24,29 +24,43 @@ struct KernelSet {
     int max_warps;       // warps per block the kernel is built for (its launch bound / 32)
 };
 
+// Kernels and sizes for (T, head_dim, heads per tile). 16-bit tiles of 8
+// heads always run on tensor cores; tiles of 4 do when `tc` is set (the
+// caller's choice for long per-warp work, where the tensor-core kernel's
+// leaner step wins; for short work the CUDA-core kernel starts faster).
 template <typename T>
-bool lookup_kernels_t(int D, int G, KernelSet* ks) {
+bool lookup_kernels_t(int D, int G, KernelSet* ks, bool tc) {
     constexpr bool kHalf = sizeof(T) == 2;
+#define PD_MMA(DD)                                                                      \
+    {                                                                                   \
+        ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, 0>);         \
+        ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                     \
+        ks->rows_per_stage = kMmaRows;                                                  \
+        ks->mma = 1;                                                                    \
+        ks->part_heads = 8;                                                             \
+        ks->smem_slack = 1024;                                                          \
+        ks->max_warps = 8;                                                              \
+    }
+#define PD_CC(DD, GG)                                                                   \
+    {                                                                                   \
+        ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);         \
+        ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                    \
+        ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                       \
+        ks->mma = 0;                                                                    \
+        ks->part_heads = GG;                                                            \
+        ks->smem_slack = 0;                                                             \
+        ks->max_warps = 8;                                                              \
+    }
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
         ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>);        \
         ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>);   \
         if constexpr (kHalf && GG == 8) {                                               \
-            ks->decode = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, 0>);     \
-            ks->warp_bytes = CfgMma<T, DD>::kWarpBytes;                                 \
-            ks->rows_per_stage = kMmaRows;                                              \
-            ks->mma = 1;                                                                \
-            ks->part_heads = 8;                                                         \
-            ks->smem_slack = 1024;                                                      \
-            ks->max_warps = 8;                                                          \
+            PD_MMA(DD)                                                                  \
+        } else if constexpr (kHalf && GG == 4) {                                        \
+            if (tc) PD_MMA(DD) else PD_CC(DD, GG)                                       \
         } else {                                                                        \
-            ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, 0>);     \
-            ks->warp_bytes = Cfg<T, DD, GG>::kWarpBytes;                                \
-            ks->rows_per_stage = Cfg<T, DD, GG>::kRC;                                   \
-            ks->mma = 0;                                                                \
-            ks->part_heads = GG;                                                        \
-            ks->smem_slack = 0;                                                         \
-            ks->max_warps = 8;                                                          \
+            PD_CC(DD, GG)                                                               \
         }                                                                               \
         return true;                                                                    \
     }
@@ -54,6 +68,8 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
     PD_CASE(128, 1) PD_CASE(128, 2) PD_CASE(128, 4) PD_CASE(128, 8)
     PD_CASE(256, 1) PD_CASE(256, 2) PD_CASE(256, 4) PD_CASE(256, 8)
 #undef PD_CASE
+#undef PD_CC
+#undef PD_MMA
     return false;
 }
 
@@ -62,12 +78,15 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
 // kernel of lookup_kernels_t. Each variant is instantiated in a translation
 // unit of its own, so that the variants build in parallel.
 template <typename T, int kVariant>
-bool lookup_variant_t(int D, int G, const void** fn) {
+bool lookup_variant_t(int D, int G, const void** fn, bool tc) {
     constexpr bool kHalf = sizeof(T) == 2;
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
         if constexpr (kHalf && GG == 8 && (kVariant & kVarFp8) == 0)                    \
             *fn = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>);    \
+        else if constexpr (kHalf && GG == 4 && (kVariant & kVarFp8) == 0)               \
+            *fn = tc ? reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>)  \
+                     : reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>); \
         else                                                                            \
             *fn = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>);    \
         return true;                                                                    \
