@@ -1,5 +1,8 @@
 // Batched decode attention over a paged (or contiguous) KV cache on CUDA
-// cores: the kernel for groups of up to 4 q heads per kv head, and for f32.
+// cores: the kernel for f32, for 16-bit groups of up to 4 q heads per kv head
+// when each warp's share is short (tiles of 4 with long shares run on tensor
+// cores), and, as a variant, for E4M3 pools outside the tensor-core kernel's
+// shapes.
 //
 // Work decomposition (see pd_walk.cuh). All positions of the call are cut into
 // equal contiguous ranges, one per warp of a grid that fills every SM. A warp
@@ -13,7 +16,8 @@
 // Inside a warp. The warp runs its own kStages-deep ring in shared memory.
 // Lane 0 issues 1-D bulk async copies (cp.async.bulk) of K and V page slices
 // -- in the HND layout rows [r0, r1) of one (page, kv head) are one
-// contiguous block -- plus, at the start of a request, the group's q rows.
+// contiguous block; the token-major (NHD) variant uses tensor-map boxes
+// instead -- plus, at the start of a request, the group's q rows.
 // Completion is counted in bytes on the stage's mbarrier. While one stage is
 // being consumed, the next ones are in flight.
 //
