@@ -145,23 +145,16 @@ def load_workload(name: str, rank: int = 0):
     return wl.CONFIGS[name](seed=wl.CONFIGS[name].__defaults__[0] + 100 * rank), "paged"
 
 
-def decode_kernel_name(w, mode: str = "paged", sms: int = 148) -> str:
+def decode_kernel_name(w, mode: str = "paged") -> str:
     """The decode kernel the library picks for this workload: tensor cores for
-    16-bit tiles of 5..8 q heads per kv head, and for tiles of 4 when each of
-    the ~8 warps per SM gets at least 2048 K/V rows; CUDA cores otherwise. For
-    E4M3 pools, tensor cores for tiles of 4..8 at head_dim 128 / 256."""
+    16-bit tiles of 4..8 q heads per kv head, CUDA cores otherwise; for E4M3
+    pools, tensor cores for tiles of 4..8 at head_dim 128 / 256."""
     g = w.group
     tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
-    per_tile = g // tiles
-    pad = 1 << (per_tile - 1).bit_length()
+    pad = 1 << (g // tiles - 1).bit_length()
     if mode == "paged_fp8":
         return "decode_fp8_mma_kernel" if (w.head_dim >= 128 and pad >= 4) else "decode_kernel"
-    if w.dtype == "f32" or pad < 4:
-        return "decode_kernel"
-    if pad == 8:
-        return "decode_mma_kernel"
-    rows_per_warp = int(w.table.kv_len().sum()) * w.num_kv_heads * tiles / (8 * sms)
-    return "decode_mma_kernel" if rows_per_warp >= 2048 else "decode_kernel"
+    return "decode_mma_kernel" if (w.dtype != "f32" and pad >= 4) else "decode_kernel"
 
 
 def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:
@@ -506,9 +499,7 @@ def main():
     dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
     dec_bytes = r["decode_bytes_mean"]  # the decode kernel's own bytes (no append rows)
     achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
-    import torch
-
-    kname = decode_kernel_name(w, r["mode"], torch.cuda.get_device_properties(0).multi_processor_count)
+    kname = decode_kernel_name(w, r["mode"])
     traffic = recorded_traffic(kname, w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd",
                                                  "paged_fp8": "/e4m3"}.get(r["mode"], "")))
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",

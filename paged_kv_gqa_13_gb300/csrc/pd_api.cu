@@ -15,13 +15,13 @@
 #include "pd_kernels.cuh"
 
 namespace pd {
-bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks, bool tc);
-bool lookup_kernels_f16(int head_dim, int heads, KernelSet* ks, bool tc);
-bool lookup_kernels_bf16(int head_dim, int heads, KernelSet* ks, bool tc);
-#define PD_VARIANTS(dt)                                                             \
-    bool lookup_fused_##dt(int head_dim, int heads, const void** fn, bool tc);      \
-    bool lookup_nhd_##dt(int head_dim, int heads, const void** fn, bool tc);        \
-    bool lookup_nhd_fused_##dt(int head_dim, int heads, const void** fn, bool tc);
+bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks);
+bool lookup_kernels_f16(int head_dim, int heads, KernelSet* ks);
+bool lookup_kernels_bf16(int head_dim, int heads, KernelSet* ks);
+#define PD_VARIANTS(dt)                                                    \
+    bool lookup_fused_##dt(int head_dim, int heads, const void** fn);      \
+    bool lookup_nhd_##dt(int head_dim, int heads, const void** fn);        \
+    bool lookup_nhd_fused_##dt(int head_dim, int heads, const void** fn);
 PD_VARIANTS(f32)
 PD_VARIANTS(f16)
 PD_VARIANTS(bf16)
@@ -56,14 +56,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t elem_size(pd_dtype dt) { return dt == PD_F32 ? 4 : 2; }
 
-// tc: 16-bit tiles of 4 heads on the tensor-core kernel (see plan_for_call).
-bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks, bool tc) {
+bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
     switch (dt) {
-#define PD_LOOKUP(dt)                                                                                          \
-    if (!pd::lookup_kernels_##dt(D, G, ks, tc)) return false;                                                   \
-    ks->variant[0] = ks->decode;                                                                                \
-    return pd::lookup_fused_##dt(D, G, &ks->variant[1], tc) && pd::lookup_nhd_##dt(D, G, &ks->variant[2], tc) && \
-           pd::lookup_nhd_fused_##dt(D, G, &ks->variant[3], tc);
+#define PD_LOOKUP(dt)                                                                                  \
+    if (!pd::lookup_kernels_##dt(D, G, ks)) return false;                                               \
+    ks->variant[0] = ks->decode;                                                                        \
+    return pd::lookup_fused_##dt(D, G, &ks->variant[1]) && pd::lookup_nhd_##dt(D, G, &ks->variant[2]) && \
+           pd::lookup_nhd_fused_##dt(D, G, &ks->variant[3]);
         case PD_F32: { PD_LOOKUP(f32) }
         case PD_F16: { PD_LOOKUP(f16) }
         case PD_BF16: { PD_LOOKUP(bf16) }
@@ -75,8 +74,8 @@ bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks, bool tc) {
 // Kernels for an E4M3 pool with q / o of type dt (f16 or bf16).
 bool lookup_fp8(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
     switch (dt) {
-        case PD_F16: return pd::lookup_kernels_f16(D, G, ks, false) && pd::lookup_fp8_f16(D, G, ks);
-        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks, false) && pd::lookup_fp8_bf16(D, G, ks);
+        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fp8_f16(D, G, ks);
+        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fp8_bf16(D, G, ks);
         default: return false;
     }
 }
@@ -148,20 +147,17 @@ void split_group(int g, int* tiles, int* per) {
     *per = g / t;
 }
 
-pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, bool tc,
-                             Plan* p);
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, Plan* p);
 
 // Plans depend only on the shape and the device: keep the last few so that a
 // decode loop pays the occupancy query and the attribute set-up once.
 // fp8: the K/V pool holds E4M3 codes (dt is then the type of q and o).
-// tc: 16-bit tiles of 4 heads on the tensor-core kernel.
-pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p, bool fp8 = false,
-                    bool tc = false) {
+pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, Plan* p, bool fp8 = false) {
     struct Entry {
         int dev;
         pd_dtype dt;
         int batch, Hq, Hk, D;
-        bool contiguous, fp8, tc;
+        bool contiguous, fp8;
         Plan plan;
     };
     static Entry cache[16];
@@ -173,23 +169,22 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
         for (int i = 0; i < used; ++i) {
             const Entry& e = cache[i];
             if (e.dev == dev && e.dt == dt && e.batch == batch && e.Hq == Hq && e.Hk == Hk && e.D == D &&
-                e.contiguous == contiguous && e.fp8 == fp8 && e.tc == tc) {
+                e.contiguous == contiguous && e.fp8 == fp8) {
                 *p = e.plan;
                 return PD_OK;
             }
         }
     }
-    const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, fp8, tc, p);
+    const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, fp8, p);
     if (st != PD_OK) return st;
     std::lock_guard<std::mutex> lk(g_mu);
-    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, fp8, tc, *p};
+    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, fp8, *p};
     next = (next + 1) % 16;
     if (used < 16) ++used;
     return PD_OK;
 }
 
-pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, bool tc,
-                             Plan* p) {
+pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, Plan* p) {
     if (dt != PD_F32 && dt != PD_F16 && dt != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || Hq <= 0 || Hk <= 0) return fail(PD_ERR_INVALID, "batch, num_qo_heads and num_kv_heads must be positive");
     if (Hq % Hk != 0) return fail(PD_ERR_INVALID, "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", Hq, Hk);
@@ -199,7 +194,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->G = 1;
     while (p->G < p->heads_per_tile) p->G *= 2;
     if (fp8 && dt == PD_F32) return fail(PD_ERR_UNSUPPORTED, "E4M3 pools take f16 or bf16 q and o");
-    if (!(fp8 ? lookup_fp8(dt, D, p->G, &p->ks) : lookup(dt, D, p->G, &p->ks, tc)))
+    if (!(fp8 ? lookup_fp8(dt, D, p->G, &p->ks) : lookup(dt, D, p->G, &p->ks)))
         return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
     p->G = p->ks.part_heads;  // the partial-result layout of the chosen kernel
     DeviceInfo di;
@@ -230,36 +225,6 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
     p->ws_bytes = p->o_off + size_t(p->slots) * p->G * D * 4;
     return PD_OK;
-}
-
-// K/V rows per warp (at most; pages may be partly filled) from which 16-bit
-// tiles of 4 heads run on the tensor-core kernel. Its step is leaner (a
-// 16-row chunk costs ~300 instructions against ~770 on CUDA cores), which wins
-// when each warp streams many rows; the CUDA-core kernel reaches its first data
-// sooner, which wins when each warp has a few hundred (measured on GB300:
-// 128k-token requests 341 -> 328 us per decode kernel on tensor cores, the
-// Llama-shaped batch, ~530 rows per warp, 60 -> 64 us).
-constexpr long long kTcMinRowsPerWarp = 2048;
-
-// The plan for one call over n_pos positions of rows_per_pos rows per (kv
-// head, head tile) pass.
-pd_status plan_for_call(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8, long long n_pos,
-                        long long rows_per_pos, Plan* p) {
-    pd_status st = make_plan(dt, batch, Hq, Hk, D, contiguous, p, fp8, false);
-    if (st != PD_OK || fp8 || dt == PD_F32 || p->G != 4) return st;
-    const long long total_rows = (long long)p->head_tiles * Hk * n_pos * rows_per_pos;
-    if (total_rows < kTcMinRowsPerWarp * p->total_warps) return PD_OK;
-    return make_plan(dt, batch, Hq, Hk, D, contiguous, p, fp8, true);
-}
-
-// Workspace bytes that fit every plan a call of this shape may take.
-size_t workspace_bytes_for(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguous, bool fp8) {
-    Plan p, q;
-    if (make_plan(dt, batch, Hq, Hk, D, contiguous, &p, fp8, false) != PD_OK) return 0;
-    size_t n = p.ws_bytes;
-    if (!fp8 && dt != PD_F32 && p.G == 4 && make_plan(dt, batch, Hq, Hk, D, contiguous, &q, fp8, true) == PD_OK)
-        n = q.ws_bytes > n ? q.ws_bytes : n;
-    return n;
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -565,16 +530,18 @@ int pd_version(void) { return PD_VERSION; }
 const char* pd_last_error_string(void) { return g_err; }
 
 size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim, pd_dtype dtype) {
-    const size_t n = workspace_bytes_for(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, false);
-    if (n) ok();
-    return n;
+    Plan p;
+    if (make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &p) != PD_OK) return 0;
+    ok();
+    return p.ws_bytes;
 }
 
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                                             pd_dtype dtype) {
-    const size_t n = workspace_bytes_for(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, false);
-    if (n) ok();
-    return n;
+    Plan p;
+    if (make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, &p) != PD_OK) return 0;
+    ok();
+    return p.ws_bytes;
 }
 
 // The paged decode, with the fused append when k_new / v_new are not null,
@@ -603,8 +570,7 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     if (!aligned(lse, 4) || !aligned(indptr, 4) || !aligned(last_page_len, 4) || (indices && !aligned(indices, 4)))
         return fail(PD_ERR_UNSUPPORTED, "lse, indices, indptr and last_page_len must be 4-byte aligned");
     Plan pl;
-    pd_status st =
-        plan_for_call(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, fp8, num_indices, page_size, &pl);
+    pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl, fp8);
     if (st != PD_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, pl.ws_bytes)) != PD_OK) return st;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -708,10 +674,6 @@ static pd_status contiguous_decode_impl(const void* q, const void* k_new, const 
     Plan pl;
     pd_status st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, &pl);
     if (st != PD_OK) return st;
-    // rows per warp decide the kernel (plan_for_call); positions follow from the chosen plan
-    if ((st = plan_for_call(dtype, batch, num_qo_heads, num_kv_heads, head_dim, true, false, batch, valid_kv_len,
-                            &pl)) != PD_OK)
-        return st;
     if ((st = check_workspace(workspace, workspace_bytes, pl.ws_bytes)) != PD_OK) return st;
     const int vpage = 4 * pl.ks.rows_per_stage;  // rows per work position
     const int npv = (valid_kv_len + vpage - 1) / vpage;
@@ -917,7 +879,7 @@ pd_status pd_merge_states(const float* o_parts, const float* lse_parts, int num_
     if (!aligned(o_parts, 16) || !aligned(o, 16)) return fail(PD_ERR_UNSUPPORTED, "o_parts and o must be 16-byte aligned");
     if (num_rows == 0) return ok();
     pd::KernelSet ks{};
-    if (!lookup(dtype, head_dim, 1, &ks, false)) return fail(PD_ERR_UNSUPPORTED, "no merge kernel for this head_dim");
+    if (!lookup(dtype, head_dim, 1, &ks)) return fail(PD_ERR_UNSUPPORTED, "no merge kernel for this head_dim");
     const void* fn = ks.merge_states;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned((num_rows + 3) / 4));
@@ -1055,9 +1017,7 @@ extern "C" pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, 
     pd_status st = noalloc_scratch(&scratch);
     if (st != PD_OK) return st;
     Plan pl;
-    if ((st = plan_for_call(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, false, num_indices, page_size,
-                            &pl)) != PD_OK)
-        return st;
+    if ((st = make_plan(dtype, batch, num_qo_heads, num_kv_heads, head_dim, false, &pl)) != PD_OK) return st;
     if (pl.ws_bytes > kNoAllocScratchBytes)
         return fail(PD_ERR_WORKSPACE,
                     "this shape needs %zu bytes of decode scratch; pd_paged_decode_noalloc has %zu "

@@ -40,8 +40,8 @@ struct CfgMma {
     static constexpr int kBoxes = D / 64;               // 64-column (128-byte) boxes per row block
     static constexpr int kBoxBytes = kMmaRows * 128;    // one box: 16 rows x 128 bytes
     static constexpr int kKBytes = kBoxes * kBoxBytes;  // K (and V) bytes of one chunk
-    static constexpr int kQBytes = 8 * D * 2;
-    static constexpr int kStageBytes = round_up(2 * kKBytes + kQBytes, 1024);
+    // q is not staged: it is read at a segment start, from L2 (see produce)
+    static constexpr int kStageBytes = round_up(2 * kKBytes, 1024);
     static constexpr int kMetaOff = kStages * kStageBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 16;
     static constexpr int kWarpBytes = round_up(kBarOff + kStages * 8, 1024);
@@ -134,8 +134,11 @@ __global__ void __launch_bounds__(256, 1)
         meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
         // A box always lands whole (rows outside the tensor are zero-filled).
         const uint32_t kv_bytes = ck.rows > 0 ? uint32_t(C::kKBytes) : 0u;
-        const uint32_t q_bytes = (ck.flags & kSegStart) ? uint32_t(GT * row_bytes) : 0u;
-        const uint32_t total = 2 * kv_bytes + q_bytes;
+        // A segment's q rows are pulled into L2 with its first chunk; the
+        // consumer reads them from there when it reaches that chunk.
+        if (ck.flags & kSegStart)
+            bulk_prefetch_l2(static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes, uint32_t(GT * row_bytes));
+        const uint32_t total = 2 * kv_bytes;
         if (total == 0) {
             mbar_arrive(bar);
             return;
@@ -149,9 +152,6 @@ __global__ void __launch_bounds__(256, 1)
                 tma_load_4d(st + C::kKBytes + bx * C::kBoxBytes, &tmv, bx * 64, c1, c2, ck.slab, bar, policy);
             }
         }
-        if (q_bytes)
-            bulk_g2s(st + 2 * C::kKBytes, static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes, q_bytes,
-                     bar);
     };
 
     // ---- consumer state: lane (g, c) owns tokens g, g+8 and heads 2c, 2c+1
@@ -228,11 +228,11 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t vs = ks + C::kKBytes;
         uint8_t* stp = wsm + slot * C::kStageBytes;
         if (m.y & kSegStart) {
-            const uint8_t* qb = stp + 2 * C::kKBytes + g * D * 2;
+            const uint8_t* qb = static_cast<const uint8_t*>(a.q) + (size_t(m.z) + g) * row_bytes;
 #pragma unroll
             for (int kk = 0; kk < kKS; ++kk) {
-                qf[kk][0] = g < GT ? *reinterpret_cast<const uint32_t*>(qb + (16 * kk + 2 * c) * 2) : 0u;
-                qf[kk][1] = g < GT ? *reinterpret_cast<const uint32_t*>(qb + (16 * kk + 2 * c + 8) * 2) : 0u;
+                qf[kk][0] = g < GT ? __ldg(reinterpret_cast<const uint32_t*>(qb + (16 * kk + 2 * c) * 2)) : 0u;
+                qf[kk][1] = g < GT ? __ldg(reinterpret_cast<const uint32_t*>(qb + (16 * kk + 2 * c + 8) * 2)) : 0u;
             }
         }
         const int rows = m.x;

@@ -24,12 +24,11 @@ struct KernelSet {
     int max_warps;       // warps per block the kernel is built for (its launch bound / 32)
 };
 
-// Kernels and sizes for (T, head_dim, heads per tile). 16-bit tiles of 8
-// heads always run on tensor cores; tiles of 4 do when `tc` is set (the
-// caller's choice for long per-warp work, where the tensor-core kernel's
-// leaner step wins; for short work the CUDA-core kernel starts faster).
+// Kernels and sizes for (T, head_dim, heads per tile): 16-bit tiles of 4 to
+// 8 heads on tensor cores (a 16-row chunk costs ~300 instructions there
+// against ~770 on CUDA cores at 4 heads), the rest on CUDA cores.
 template <typename T>
-bool lookup_kernels_t(int D, int G, KernelSet* ks, bool tc) {
+bool lookup_kernels_t(int D, int G, KernelSet* ks) {
     constexpr bool kHalf = sizeof(T) == 2;
 #define PD_MMA(DD)                                                                      \
     {                                                                                   \
@@ -55,10 +54,8 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks, bool tc) {
     if (D == DD && G == GG) {                                                           \
         ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>);        \
         ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>);   \
-        if constexpr (kHalf && GG == 8) {                                               \
+        if constexpr (kHalf && GG >= 4) {                                               \
             PD_MMA(DD)                                                                  \
-        } else if constexpr (kHalf && GG == 4) {                                        \
-            if (tc) PD_MMA(DD) else PD_CC(DD, GG)                                       \
         } else {                                                                        \
             PD_CC(DD, GG)                                                               \
         }                                                                               \
@@ -78,15 +75,12 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks, bool tc) {
 // kernel of lookup_kernels_t. Each variant is instantiated in a translation
 // unit of its own, so that the variants build in parallel.
 template <typename T, int kVariant>
-bool lookup_variant_t(int D, int G, const void** fn, bool tc) {
+bool lookup_variant_t(int D, int G, const void** fn) {
     constexpr bool kHalf = sizeof(T) == 2;
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
-        if constexpr (kHalf && GG == 8 && (kVariant & kVarFp8) == 0)                    \
+        if constexpr (kHalf && GG >= 4 && (kVariant & kVarFp8) == 0)                    \
             *fn = reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>);    \
-        else if constexpr (kHalf && GG == 4 && (kVariant & kVarFp8) == 0)               \
-            *fn = tc ? reinterpret_cast<const void*>(decode_mma_kernel<T, DD, kVariant>)  \
-                     : reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>); \
         else                                                                            \
             *fn = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVariant>);    \
         return true;                                                                    \

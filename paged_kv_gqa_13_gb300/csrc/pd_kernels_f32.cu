@@ -2,7 +2,7 @@
 #include "pd_kernels.cuh"
 
 namespace pd {
-bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks, bool tc) {
-    return lookup_kernels_t<float>(head_dim, heads, ks, tc);
+bool lookup_kernels_f32(int head_dim, int heads, KernelSet* ks) {
+    return lookup_kernels_t<float>(head_dim, heads, ks);
 }
 }  // namespace pd

@@ -2,7 +2,7 @@
 #include "pd_kernels.cuh"
 
 namespace pd {
-bool lookup_nhd_fused_f32(int head_dim, int heads, const void** fn, bool tc) {
-    return lookup_variant_t<float, 3>(head_dim, heads, fn, tc);
+bool lookup_nhd_fused_f32(int head_dim, int heads, const void** fn) {
+    return lookup_variant_t<float, 3>(head_dim, heads, fn);
 }
 }  // namespace pd
