@@ -340,9 +340,24 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     if (!prof) plk.unlock();
     cudaError_t e;
     if (a.total_pos > 0) {
-        a.pos_per_warp = (a.total_pos + pl.total_warps - 1) / pl.total_warps;
-        const long long warps_used = (a.total_pos + a.pos_per_warp - 1) / a.pos_per_warp;
-        const int grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
+        const long long passes = a.total_pos / a.n_pos;
+        int grid;
+        if (nhd && passes == pl.nwarps && (long long)a.n_pos + pl.ctas <= 0x7fffffffLL) {
+            // Token-major cache: block c's warp k takes range c of pass k, so
+            // that one SM reads all kv heads of a token range at about the same
+            // time (each kv head's rows are 256 B pieces of every token block).
+            // Passes are padded to whole units; padding positions hold no request.
+            const long long w = pl.ctas;
+            a.pos_per_warp = (a.n_pos + w - 1) / w;
+            a.n_pos = int(w * a.pos_per_warp);
+            a.total_pos = passes * a.n_pos;
+            a.unit_transpose = 1;
+            grid = int(w);
+        } else {
+            a.pos_per_warp = (a.total_pos + pl.total_warps - 1) / pl.total_warps;
+            const long long warps_used = (a.total_pos + a.pos_per_warp - 1) / a.pos_per_warp;
+            grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
+        }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(pl.nwarps * 32);

@@ -92,7 +92,9 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t wsm_u32 = smem_u32(wsm);
     const uint32_t bar0 = wsm_u32 + C::kBarOff;
 
-    const long long gwarp = (long long)blockIdx.x * nwarps + wid;
+    // This warp's unit (see DecodeArgs::unit_transpose).
+    const long long gwarp = a.unit_transpose ? (long long)wid * gridDim.x + blockIdx.x
+                                             : (long long)blockIdx.x * nwarps + wid;
     const long long p0 = gwarp * a.pos_per_warp;
     const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);

@@ -397,6 +397,11 @@ struct DecodeArgs {
     const float* k_scale;
     const float* v_scale;
     int test_extra_tx;  // test-only wait-timeout injection (pd_test_inject_wait_timeout); normally 0
+    // 0: warp w of block c holds unit c * warps_per_block + w. 1: unit
+    // w * blocks + c, with one pass per warp of a block and passes padded to a
+    // whole number of units, so that a block's warps hold the same token range
+    // of every pass (token-major contiguous cache).
+    int unit_transpose;
 };
 
 struct MergeArgs {

@@ -191,6 +191,7 @@ struct Walk {
         long long rows;
         if (contiguous) {
             const int b = i / a.npv;
+            if (b >= a.batch) return;  // a padding position (unit_transpose)
             const long long r0 = (long long)(i % a.npv) * a.vpage;
             rows = min((long long)a.vpage, a.slab_rows - r0);
             row = kv_row<kNhd>(a, b, kh, r0);

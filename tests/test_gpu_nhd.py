@@ -1,6 +1,6 @@
 """GPU parity for the token-major (NHD) contiguous cache, [batch, max_kv_len, Hk, D]:
-decode against the oracle and bitwise against the HND entry on the transposed
-cache; append and fused append + decode bit-exact against the oracle."""
+decode against the oracle and against the HND entry on the transposed cache;
+append and fused append + decode bit-exact against the oracle."""
 import math
 
 import numpy as np
@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests.gpu_helpers import compare, to_dev, to_host_raw
+from tests.gpu_helpers import LSE_TOL, O_TOL, compare, to_dev, to_host_raw
 
 pytestmark = pytest.mark.gpu
 
@@ -51,12 +51,20 @@ def test_nhd_decode_matches_oracle_and_hnd(dtype, Hq, Hk, D, L, valid):
     ws = pd.alloc_workspace(pd.pd_contiguous_decode_workspace_bytes(B, Hq, Hk, D, CODE[dtype]))
     pd.pd_contiguous_decode_nhd(qd, kd, vd, o, lse, valid, scale, ws)
     compare(o, lse, o_ref, lse_ref, dtype, "nhd")
-    # the same values in HND order go through the same arithmetic
+    # The same values in HND order. When the passes fill a block's warps the
+    # NHD entry lays its units out per token range, so requests split at other
+    # points than in HND order and partial sums round differently: equal within
+    # the tolerance, and bit-identical across repeated NHD calls.
     o2 = torch.empty_like(qd)
     l2 = torch.empty_like(lse)
     pd.pd_contiguous_decode(qd, kd.transpose(1, 2).contiguous(), vd.transpose(1, 2).contiguous(), o2, l2, valid,
                             scale, ws)
-    assert torch.equal(_raw(o, dtype), _raw(o2, dtype)) and torch.equal(lse, l2)
+    assert float((o.double() - o2.double()).abs().max()) <= 2 * O_TOL[dtype]
+    assert float((lse.double() - l2.double()).abs().max()) <= 2 * LSE_TOL
+    o3 = torch.empty_like(qd)
+    l3 = torch.empty_like(lse)
+    pd.pd_contiguous_decode_nhd(qd, kd, vd, o3, l3, valid, scale, ws)
+    assert torch.equal(_raw(o, dtype), _raw(o3, dtype)) and torch.equal(lse, l3)
     assert pd.pd_read_device_flags(ws) == 0
 
 
