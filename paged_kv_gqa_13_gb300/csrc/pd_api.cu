@@ -249,30 +249,34 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // {head_dim, kv heads, rows, slabs} (NHD). `rows` is the extent read (page
 // size, or the valid length of a contiguous cache), `slab_rows` the rows
 // allocated per (slab, kv head) that set the strides; rows past `rows` read as
-// zero. mma: boxes of 64 columns x 16 rows with the 128-byte swizzle (the
-// tensor-core kernel). Otherwise: unswizzled boxes of head_dim columns x
-// `box_rows` rows (the CUDA-core kernel on an NHD cache). A box holds rows of
-// one kv head, so it lands as consecutive rows either way.
+// zero. mma 1: boxes of 64 16-bit columns x 16 rows with the 128-byte
+// swizzle (the tensor-core kernel); mma 2: the same for E4M3 codes, 128
+// one-byte columns (the E4M3 tensor-core kernel). mma 0: unswizzled boxes of
+// head_dim columns x `box_rows` rows (the CUDA-core kernel on an NHD cache).
+// A box holds rows of one kv head, so it lands as consecutive rows either way.
 pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long rows, long long slab_rows,
-                      int Hk, long long slabs, bool nhd, bool mma, int box_rows) {
+                      int Hk, long long slabs, bool nhd, int mma, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t row = cuuint64_t(D) * elem_size(dt);
+    // mma 2: E4M3 codes, one byte per element, whatever the type of q and o
+    const cuuint64_t row = cuuint64_t(D) * (mma == 2 ? 1u : elem_size(dt));
     const cuuint64_t dims_hnd[4] = {cuuint64_t(D), cuuint64_t(rows), cuuint64_t(Hk), cuuint64_t(slabs)};
     const cuuint64_t dims_nhd[4] = {cuuint64_t(D), cuuint64_t(Hk), cuuint64_t(rows), cuuint64_t(slabs)};
     const cuuint64_t str_hnd[3] = {row, cuuint64_t(slab_rows) * row, cuuint64_t(Hk) * slab_rows * row};
     const cuuint64_t str_nhd[3] = {row, cuuint64_t(Hk) * row, cuuint64_t(Hk) * slab_rows * row};
     const cuuint64_t* dims = nhd ? dims_nhd : dims_hnd;
     const cuuint64_t* strides = nhd ? str_nhd : str_hnd;
-    const cuuint32_t cols = mma ? 64u : cuuint32_t(D);
+    // a swizzled box row is 128 bytes: 64 16-bit or 128 E4M3 elements
+    const cuuint32_t cols = mma == 2 ? 128u : mma ? 64u : cuuint32_t(D);
     const cuuint32_t brows = mma ? cuuint32_t(pd::kMmaRows) : cuuint32_t(box_rows);
     const cuuint32_t box_hnd[4] = {cols, brows, 1, 1};
     const cuuint32_t box_nhd[4] = {cols, 1, brows, 1};
     const cuuint32_t* box = nhd ? box_nhd : box_hnd;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUtensorMapDataType ty = dt == PD_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                   : dt == PD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapDataType ty = mma == 2        ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dt == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == PD_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const CUresult r = enc(map, ty, 4, const_cast<void*>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -327,7 +331,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     std::memset(maps, 0, sizeof(maps));
     if ((pl.ks.mma || nhd) && a.total_pos > 0) {
         const long long rows = a.contiguous ? a.valid_kv_len : a.slab_rows;
-        const bool mma = pl.ks.mma != 0;
+        const int mma = pl.ks.mma;
         pd_status st = make_kv_map(&maps[0], a.k, dt, D, rows, a.slab_rows, a.num_kv_heads, slabs, nhd, mma,
                                    pl.ks.rows_per_stage);
         if (st == PD_OK)

@@ -8,14 +8,18 @@
 // step's fixed work (barrier wait, walk, softmax bookkeeping) than the page's
 // bytes take to arrive. This kernel therefore:
 //  - stages up to two pages of the same segment per pipeline slot at head_dim
-//    128 (32 tokens, two independent 16-token score tiles), by 1-D bulk
-//    copies of the pages' contiguous rows;
+//    128 (32 tokens, two independent 16-token score tiles). The codes come
+//    through tensor maps in boxes of 16 rows x 128 bytes with the 128-byte
+//    swizzle (16-byte piece x of row r lands at piece x ^ (r & 7)), which
+//    keeps the reads below free of bank conflicts;
 //  - builds the K operand of the score mma straight from the codes in shared
 //    memory, widening them in registers (every E4M3 value is an f16 value, so
 //    the f16 mma sees them exactly). The 16 dims of k step kk = 4j + t that
 //    lane (g, c) holds are not the mma's canonical columns but dims
-//    64j + 16c + 4t + {0..3}: one 16-byte load per row feeds four k steps. q
-//    takes the same permutation, so the dot products are unchanged;
+//    k_base(c, j) + 4t + {0..3}, k_base = 128 (j >> 1) + 32c + 16 (j & 1):
+//    one 16-byte load per row feeds four k steps, and the 8 lanes of rows g
+//    and g + 1 (one load phase) read 8 different 16-byte pieces. q takes the
+//    same permutation, so the dot products are unchanged;
 //  - builds the V operand of the P.V mma from the codes in the same way: the
 //    accumulator rows of m tile mt = 4q + u stand for dims 64q + 4g + u
 //    (row g) and 64q + 32 + 4g + u (row g + 8), so that a lane reads 4
@@ -50,20 +54,24 @@ struct CfgF8 {
     // stage), one at 256 (a tile is 4 KB already).
     static constexpr int kSub = D <= 128 ? 2 : 1;
     static constexpr int kTileRaw = kMmaRows * D;      // E4M3 bytes of one K (or V) tile
+    static constexpr int kBoxes = D / 128;             // 128-byte column boxes per tile
+    static constexpr int kBoxBytes = kMmaRows * 128;   // one box: 16 rows x 128 codes
 
     static constexpr int kVOff = kSub * kTileRaw;      // V tiles within a stage
     // q is not staged: it is read at a segment start, from L2 (see produce)
     static constexpr int kStageBytes = round_up(2 * kSub * kTileRaw, 128);
     static constexpr int kMetaOff = kStages * kStageBytes;
     static constexpr int kBarOff = kMetaOff + kStages * 16;
-    static constexpr int kWarpBytes = round_up(kBarOff + kStages * 8, 128);
+    // stages stay 1024-byte aligned for the swizzle
+    static constexpr int kWarpBytes = round_up(kBarOff + kStages * 8, 1024);
     static constexpr int kKSteps = D / 16;
     static constexpr int kJ = D / 64;  // 64-dim groups: one 16-byte load per row each
 };
 
 template <typename T, int D>
 __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
-    decode_fp8_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap) {
+    decode_fp8_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
     static_assert(D == 128 || D == 256, "head_dim 128 or 256");
     using C = CfgF8<D>;
     using M = __half;  // mma operand type
@@ -72,7 +80,9 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     constexpr float kTauM = 8.0f;
     const float kNegInf = -__int_as_float(0x7f800000);
 
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Swizzled TMA boxes want 1024-byte aligned destinations.
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -89,6 +99,10 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     Walk<false> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
+    if (lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
 
     walk.stage_table(s_indptr, s_lpl, [&] {
         if (lane == 0) {
@@ -123,27 +137,31 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         const int r1 = two ? c1.rows : 0;
         const int flags = two ? ((c0.flags & ~kSegEnd) | (c1.flags & kSegEnd)) : c0.flags;
         meta[slot] = make_int4(c0.rows | (r1 << 16), flags, c0.qrow, c0.seg);
-        const uint32_t b0 = uint32_t(c0.rows) * uint32_t(D), b1 = uint32_t(r1) * uint32_t(D);
         // A segment's q rows are pulled into L2 with its first stage; the
         // consumer reads them from there when it reaches that stage.
         if (flags & kSegStart)
             bulk_prefetch_l2(static_cast<const uint8_t*>(a.q) + size_t(c0.qrow) * q_row_bytes,
                              uint32_t(GT * q_row_bytes));
-        const uint32_t total = 2 * (b0 + b1);
+        // A tile with rows lands as whole boxes (rows outside the page read as zero).
+        const int n0 = c0.rows > 0, n1 = r1 > 0;
+        const uint32_t total = uint32_t(n0 + n1) * 2u * uint32_t(C::kTileRaw);
         if (total == 0) {
             mbar_arrive(bar);
             return;
         }
         mbar_arrive_expect_tx(bar, total + extra_tx);
-        if (b0) {
-            const size_t off = kv_row<false>(a, c0.slab, c0.kh, c0.row0) * size_t(D);
-            bulk_g2s(st, static_cast<const uint8_t*>(a.k) + off, b0, bar, policy);
-            bulk_g2s(st + C::kVOff, static_cast<const uint8_t*>(a.v) + off, b0, bar, policy);
-        }
-        if (b1) {
-            const size_t off = kv_row<false>(a, c1.slab, c1.kh, c1.row0) * size_t(D);
-            bulk_g2s(st + C::kTileRaw, static_cast<const uint8_t*>(a.k) + off, b1, bar, policy);
-            bulk_g2s(st + C::kVOff + C::kTileRaw, static_cast<const uint8_t*>(a.v) + off, b1, bar, policy);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+            if (n0) {
+                tma_load_4d(st + bx * C::kBoxBytes, &tmk, bx * 128, c0.row0, c0.kh, c0.slab, bar, policy);
+                tma_load_4d(st + C::kVOff + bx * C::kBoxBytes, &tmv, bx * 128, c0.row0, c0.kh, c0.slab, bar, policy);
+            }
+            if (n1) {
+                tma_load_4d(st + C::kTileRaw + bx * C::kBoxBytes, &tmk, bx * 128, c1.row0, c1.kh, c1.slab, bar,
+                            policy);
+                tma_load_4d(st + C::kVOff + C::kTileRaw + bx * C::kBoxBytes, &tmv, bx * 128, c1.row0, c1.kh,
+                            c1.slab, bar, policy);
+            }
         }
     };
 
@@ -224,12 +242,13 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         const int rows[2] = {m.x & 0xffff, m.x >> 16};
         if (m.y & kSegStart) {
             // q of head g at the permuted dims of k step kk = 4j + t:
-            // 64j + 16c + 4t + {0, 1} (first register), + {2, 3} (second).
+            // k_base(c, j) + 4t + {0, 1} (first register), + {2, 3} (second).
             const float qs = a.q_scale * __ldg(a.k_scale + (m.z % a.num_qo_heads) / a.group);
             const uint8_t* qb = static_cast<const uint8_t*>(a.q) + (size_t(m.z) + g) * q_row_bytes;
 #pragma unroll
             for (int kk = 0; kk < kKS; ++kk) {
-                const int d0 = 64 * (kk >> 2) + 16 * c + 4 * (kk & 3);
+                const int j = kk >> 2;
+                const int d0 = 128 * (j >> 1) + 32 * c + 16 * (j & 1) + 4 * (kk & 3);
                 uint2 w = make_uint2(0u, 0u);
                 if (g < GT) w = __ldg(reinterpret_cast<const uint2*>(qb + d0 * 2));
                 const uint32_t ww[2] = {w.x, w.y};
@@ -257,9 +276,11 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             uint32_t xa[2][4], xb[2][4];
 #pragma unroll
             for (int s = 0; s < C::kSub; ++s) {
-                const uint8_t* kr = stp + s * C::kTileRaw + 16 * c + 64 * j;
-                const uint4 wa = *reinterpret_cast<const uint4*>(kr + g * D);
-                const uint4 wb = *reinterpret_cast<const uint4*>(kr + (g + 8) * D);
+                // rows g and g + 8 of the box holding this 16-byte piece (2c + (j & 1))
+                const uint8_t* kr = stp + s * C::kTileRaw + (j >> 1) * C::kBoxBytes + g * 128 +
+                                    (((2 * c + (j & 1)) ^ g) << 4);
+                const uint4 wa = *reinterpret_cast<const uint4*>(kr);
+                const uint4 wb = *reinterpret_cast<const uint4*>(kr + 8 * 128);
                 xa[s][0] = wa.x, xa[s][1] = wa.y, xa[s][2] = wa.z, xa[s][3] = wa.w;
                 xb[s][0] = wb.x, xb[s][1] = wb.y, xb[s][2] = wb.z, xb[s][3] = wb.w;
             }
@@ -337,17 +358,22 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s) {
             if (rows[s] == 0) continue;
-            const uint8_t* vr = stp + C::kVOff + s * C::kTileRaw + 4 * g;
+            const uint8_t* vt = stp + C::kVOff + s * C::kTileRaw + 4 * (g & 3);
             const int t0 = 2 * c;
 #pragma unroll
             for (int q = 0; q < C::kJ; ++q) {
+                // dims 64q + 32h + 4g + {0..3}: 16-byte piece 4 (q & 1) + 2h + (g >> 2)
+                // of box q >> 1, at piece ^ (token & 7) in shared memory
+                const uint8_t* vb = vt + (q >> 1) * C::kBoxBytes;
                 uint32_t w[4][2];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tk = t0 + (i & 1) + 8 * (i >> 1);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        w[i][h] = tk < rows[s] ? *reinterpret_cast<const uint32_t*>(vr + tk * D + 64 * q + 32 * h) : 0u;
+                    for (int h = 0; h < 2; ++h) {
+                        const int piece = (4 * (q & 1) + 2 * h + (g >> 2)) ^ (tk & 7);
+                        w[i][h] = tk < rows[s] ? *reinterpret_cast<const uint32_t*>(vb + tk * 128 + (piece << 4)) : 0u;
+                    }
                 }
                 // pr[pair][h][half]: bytes u of tokens (t0, t0+1) (pair 0) or
                 // (t0+8, t0+9) (pair 1), u = 2 * half + (0 | 1 in the 16-bit halves)

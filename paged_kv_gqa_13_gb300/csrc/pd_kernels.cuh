@@ -18,7 +18,7 @@ struct KernelSet {
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
     int rows_per_stage;  // K (and V) rows one pipeline stage holds
-    int mma;             // 1: K/V copies through 128B-swizzled tensor maps (tensor-core kernel, 16-bit pools)
+    int mma;             // K/V copies through 128B-swizzled tensor maps: 1 16-bit pools, 2 E4M3 pools (tensor cores)
     int part_heads;      // heads per partial-result slot: the group tile G, or 8 for the tensor-core kernel
     int smem_slack;      // extra dynamic shared memory for aligning the stages
     int max_warps;       // warps per block the kernel is built for (its launch bound / 32)
@@ -107,8 +107,9 @@ bool lookup_fp8_t(int D, int G, KernelSet* ks) {
             ks->warp_bytes = CfgF8<DD>::kWarpBytes;                                          \
             ks->rows_per_stage = kMmaRows;                                                   \
             ks->part_heads = 8;                                                              \
-            ks->smem_slack = 0;                                                              \
+            ks->smem_slack = 1024;                                                           \
             ks->max_warps = CfgF8<DD>::kMaxWarps;                                            \
+            ks->mma = 2;                                                                     \
         } else {                                                                             \
             ks->decode = reinterpret_cast<const void*>(decode_kernel<T, DD, GG, kVarFp8>);   \
             ks->warp_bytes = Cfg<T, DD, GG, 1>::kWarpBytes;                                  \
@@ -116,8 +117,8 @@ bool lookup_fp8_t(int D, int G, KernelSet* ks) {
             ks->part_heads = GG;                                                             \
             ks->smem_slack = 0;                                                              \
             ks->max_warps = 8;                                                               \
+            ks->mma = 0;                                                                     \
         }                                                                                    \
-        ks->mma = 0;                                                                         \
         ks->variant[0] = ks->decode;                                                         \
         ks->variant[1] = ks->variant[2] = ks->variant[3] = nullptr;                          \
         return true;                                                                         \
