@@ -8,78 +8,53 @@ namespace pd {
 
 // Weighted sum of partial rows, parts taken in index order: lane c of each
 // group of 32 parts computes its part's weight 2^(lse_c - L); the weights are
-// broadcast with shuffles and every lane accumulates its kPer columns.
-// kFastMax bounds the parts whose rows are all loaded before any is used, and
-// kGroup the rows in flight beyond that: the register budget of the caller.
-template <int kPer, int kFastMax = 16, int kGroup = 8, class LseAt, class RowAt>
+// broadcast with shuffles and every lane accumulates its kPer columns. Rows
+// are loaded in rounds of kRound (the caller's register budget); the first
+// round is requested together with the lse values, so up to kRound parts take
+// one round trip and every further kRound parts one more.
+template <int kPer, int kRoundMax = 16, class LseAt, class RowAt>
 __device__ __forceinline__ float merge_rows(int parts, LseAt lse_at, RowAt row_at, float* acc) {
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;
-    constexpr int kFast = (64 / kPer) < kFastMax ? (64 / kPer) : kFastMax;  // parts kept in registers
-    if (parts <= kFast) {
-        // One round trip: every part's lse and row are requested before any
-        // weight is known.
-        float rows[kFast][kPer];
+    constexpr int kRound = (64 / kPer) < kRoundMax ? (64 / kPer) : kRoundMax;  // divides 32
+    static_assert(32 % kRound == 0, "a round never straddles two groups of 32 parts");
+    float rows[kRound][kPer];
+    auto load_round = [&](int base) {
 #pragma unroll
-        for (int cp = 0; cp < kFast; ++cp) {
-            if (cp < parts) {
-                const float* po = row_at(cp) + lane * kPer;
+        for (int j = 0; j < kRound; ++j) {
+            if (base + j < parts) {
+                const float* po = row_at(base + j) + lane * kPer;
 #pragma unroll
                 for (int e = 0; e < kPer; e += 2) {
                     const float2 t = *reinterpret_cast<const float2*>(po + e);
-                    rows[cp][e] = t.x;
-                    rows[cp][e + 1] = t.y;
+                    rows[j][e] = t.x;
+                    rows[j][e + 1] = t.y;
                 }
             }
         }
-        const float mine = lane < parts ? lse_at(lane) : kNegInf;
-        const float M = warp_max(mine);
-        if (M == kNegInf) return kNegInf;
-        const float S = warp_sum(lane < parts ? ex2(mine - M) : 0.f);
-        const float L = M + log2f(S);
-        const float w_mine = lane < parts ? ex2(mine - L) : 0.f;
-#pragma unroll
-        for (int cp = 0; cp < kFast; ++cp) {
-            const float w = __shfl_sync(kFull, w_mine, cp);
-            if (cp < parts) {
-#pragma unroll
-                for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, rows[cp][e], acc[e]);
-            }
-        }
-        return L;
-    }
-    float M = kNegInf;
-    for (int cp = lane; cp < parts; cp += 32) M = fmaxf(M, lse_at(cp));
+    };
+    const float mine = lane < parts ? lse_at(lane) : kNegInf;
+    load_round(0);
+    float M = mine;
+    for (int cp = lane + 32; cp < parts; cp += 32) M = fmaxf(M, lse_at(cp));
     M = warp_max(M);
     if (M == kNegInf) return kNegInf;
-    float S = 0.f;
-    for (int cp = lane; cp < parts; cp += 32) S += ex2(lse_at(cp) - M);
+    float S = lane < parts ? ex2(mine - M) : 0.f;
+    for (int cp = lane + 32; cp < parts; cp += 32) S += ex2(lse_at(cp) - M);
     S = warp_sum(S);
     const float L = M + log2f(S);
-    for (int base = 0; base < parts; base += 32) {
-        const int n = min(32, parts - base);
-        const float w_mine = (lane < n) ? ex2(lse_at(base + lane) - L) : 0.f;
-        for (int j0 = 0; j0 < n; j0 += kGroup) {
-            float rows[kGroup][kPer];  // kGroup rows in flight before any is used
+    float w_mine = lane < parts ? ex2(mine - L) : 0.f;  // weight of part (base & ~31) + lane
+    for (int base = 0; base < parts; base += kRound) {
+        if (base > 0) {
+            if ((base & 31) == 0) w_mine = base + lane < parts ? ex2(lse_at(base + lane) - L) : 0.f;
+            load_round(base);
+        }
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                if (j0 + j < n) {
-                    const float* po = row_at(base + j0 + j) + lane * kPer;
+        for (int j = 0; j < kRound; ++j) {
+            const float w = __shfl_sync(kFull, w_mine, (base + j) & 31);
+            if (base + j < parts) {
 #pragma unroll
-                    for (int e = 0; e < kPer; e += 2) {
-                        const float2 t = *reinterpret_cast<const float2*>(po + e);
-                        rows[j][e] = t.x;
-                        rows[j][e + 1] = t.y;
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
-                if (j0 + j < n) {
-#pragma unroll
-                    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, rows[j][e], acc[e]);
-                }
+                for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, rows[j][e], acc[e]);
             }
         }
     }
@@ -107,9 +82,9 @@ __device__ __forceinline__ void store_row(T* orow, const float* acc) {
 // before waiting for the decode grid.
 template <typename T, int D>
 // Its grid follows the decode with one warp per (segment, head); registers
-// are held to 85 per thread (8 parts in registers and groups of 4 beyond, 4
-// and 2 at head_dim 256) so that 6 blocks fit per SM and the warps that remain
-// after the decode run in few waves.
+// are held to 85 per thread (rounds of 8 parts, 4 at head_dim 256) so that 6
+// blocks fit per SM and the warps that remain after the decode run in few
+// waves.
 __global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs a) {
     constexpr int kPer = D / 32;  // elements per lane
     const float kNegInf = -__int_as_float(0x7f800000);
@@ -145,7 +120,7 @@ __global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs 
         grid_dependency_wait();     // the decode kernel's partials are complete and visible
         const int parts = int(last - first + 1);
         const long long slot0 = (first + s) * a.G + h;  // slot of part c: (first + c + s) * G + h
-        L = merge_rows<kPer, (D <= 128 ? 8 : 4), (D <= 128 ? 4 : 2)>(
+        L = merge_rows<kPer, (D <= 128 ? 8 : 4)>(
             parts, [&](int cp) { return a.part_lse[slot0 + (long long)cp * a.G]; },
             [&](int cp) { return a.part_o + size_t(slot0 + (long long)cp * a.G) * D; }, acc);
     }
