@@ -74,7 +74,8 @@ typedef enum {
 #define PD_FLAG_BAD_INDPTR 0x4        /* indptr decreasing, negative or past num_indices */
 #define PD_FLAG_WAIT_TIMEOUT 0x8      /* a copy pipeline wait passed its time limit; outputs invalid */
 
-/* Bytes at the start of every workspace that hold the status word. */
+/* Bytes at the start of every workspace that hold the status word and the
+ * decode's work-distribution counters (zero between calls). */
 #define PD_WORKSPACE_HEADER_BYTES 256
 
 /*

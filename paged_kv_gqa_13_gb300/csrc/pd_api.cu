@@ -136,6 +136,7 @@ struct Plan {
     pd::KernelSet ks{};
     int table_bytes = 0, nwarps = 0, ctas = 0;
     long long total_warps = 0, segments = 0, slots = 0;
+    bool tails = false;  // the decode kernel takes DecodeArgs::tail (slots for two units per warp)
     size_t smem = 0, lse_off = 0, o_off = 0, ws_bytes = 0;
 };
 
@@ -220,7 +221,8 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->ctas = di.sms * per_sm;
     p->total_warps = (long long)p->ctas * p->nwarps;
     p->segments = (long long)p->head_tiles * Hk * batch;
-    p->slots = p->total_warps + p->segments;
+    p->tails = p->ks.mma == 1;
+    p->slots = (p->tails ? 2 : 1) * p->total_warps + p->segments;
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
     p->ws_bytes = p->o_off + size_t(p->slots) * p->G * D * 4;
@@ -320,6 +322,13 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 // Test-only: extra bytes warp 0's first pipeline stage waits for (0: off).
 std::atomic<int> g_inject_extra_tx{0};
 
+// Dynamic tails (DecodeArgs::tail): shares of at least kTailMinPos positions
+// give their last 1/kTailDiv to whichever warps finish first. The counters
+// sit in the workspace header after the status word.
+constexpr long long kTailMinPos = 12;
+constexpr long long kTailDiv = 6;
+constexpr size_t kTailCtlOff = 64;
+
 // nhd: the contiguous cache is token-major, [slabs, slab_rows, Hk, D].
 pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, bool nhd,
                         cudaStream_t stream) {
@@ -361,6 +370,13 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
             a.pos_per_warp = (a.total_pos + pl.total_warps - 1) / pl.total_warps;
             const long long warps_used = (a.total_pos + a.pos_per_warp - 1) / a.pos_per_warp;
             grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
+            // SMs stream at different rates (by up to ~25% across one GPU), so
+            // equal shares end at different times: the last kTailDiv-th of
+            // each share is handed out to the warps that finish first.
+            if (pl.tails && a.pos_per_warp >= kTailMinPos) {
+                a.tail = int(a.pos_per_warp / kTailDiv);
+                a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
+            }
         }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
@@ -391,6 +407,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     m.G = pl.G;
     m.n_pos = a.n_pos;
     m.pos_per_warp = a.pos_per_warp;
+    m.tail = a.tail;
     m.contiguous = a.contiguous;
     m.npv = a.npv;
     m.append = (a.k_new != nullptr && !a.contiguous) ? 1 : 0;

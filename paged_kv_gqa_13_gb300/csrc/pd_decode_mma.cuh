@@ -95,8 +95,11 @@ __global__ void __launch_bounds__(256, 1)
     // This warp's unit (see DecodeArgs::unit_transpose).
     const long long gwarp = a.unit_transpose ? (long long)wid * gridDim.x + blockIdx.x
                                              : (long long)blockIdx.x * nwarps + wid;
-    const long long p0 = gwarp * a.pos_per_warp;
-    const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
+    const long long ppw = a.pos_per_warp;
+    const long long p0 = gwarp * ppw;
+    const long long pend = min(p0 + ppw - a.tail, a.total_pos);  // the head of share gwarp
+    long long unit = a.tail ? 2 * gwarp : gwarp;                   // unit of the chunks being produced
+    bool tails_left = a.tail != 0;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
@@ -114,14 +117,31 @@ __global__ void __launch_bounds__(256, 1)
     });
     __syncthreads();  // the only block-wide barrier
     launch_dependents();
-    if (p0 >= pend) return;
+    if (p0 >= pend && !tails_left) return;  // with tails a warp without a head may still take some
     walk.build(p0, first_page);
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(D) * sizeof(T);
+    const long long n_shares = (a.total_pos + ppw - 1) / ppw;
     auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
-        const bool have = walk.template next<kMmaRows>(&ck);
+        bool have = walk.template next<kMmaRows>(&ck);
+        // This warp's range is done: take the next share's tail, if any is left.
+        while (!have && tails_left) {
+            unsigned t = 0;
+            if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
+            t = __shfl_sync(kFull, t, 0);
+            if ((long long)t >= n_shares) {
+                tails_left = false;
+                break;
+            }
+            const long long t0 = (long long)t * ppw + (ppw - a.tail);
+            const long long t1 = min(t0 + a.tail, a.total_pos);
+            if (t0 >= t1) continue;
+            unit = 2 * (long long)t + 1;
+            walk.restart(t0, t1);
+            have = walk.template next<kMmaRows>(&ck);
+        }
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
         if constexpr (kFused) {
@@ -133,7 +153,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar);
             return;
         }
-        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
+        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg + int(unit));  // .w: partial slot
         // A box always lands whole (rows outside the tensor are zero-filled).
         const uint32_t kv_bytes = ck.rows > 0 ? uint32_t(C::kKBytes) : 0u;
         // A segment's q rows are pulled into L2 with its first chunk; the
@@ -202,7 +222,7 @@ __global__ void __launch_bounds__(256, 1)
                 if (h1 < GT) a.lse[size_t(qrow) + h1] = lse1 == kNegInf ? kNegInf : lse1 * kLn2;
             }
         } else {
-            const long long slot = gwarp + m.w;
+            const long long slot = m.w;
             float* p0r = a.part_o + (size_t(slot) * 8 + h0) * D;
             float* p1r = p0r + D;
 #pragma unroll
@@ -336,6 +356,18 @@ __global__ void __launch_bounds__(256, 1)
         consume(slot, m);
         __syncwarp();
         produce(slot, 0u);
+    }
+    if (a.tail != 0 && lane == 0) {
+        // Every warp of the grid passes here once; the last one resets the
+        // tail counters for the next call (no grab can follow: every warp
+        // has stopped taking tails before it counts itself finished).
+        __threadfence();
+        const unsigned warps = gridDim.x * unsigned(nwarps);
+        if (atomicAdd(a.tail_ctl + 1, 1u) == warps - 1u) {
+            __threadfence();
+            atomicExch(a.tail_ctl, 0u);
+            atomicExch(a.tail_ctl + 1, 0u);
+        }
     }
 }
 

@@ -402,6 +402,15 @@ struct DecodeArgs {
     // whole number of units, so that a block's warps hold the same token range
     // of every pass (token-major contiguous cache).
     int unit_transpose;
+    // Positions at the end of each warp's share (pos_per_warp) that its warp
+    // does not run: they form one more unit per share, handed out in share
+    // order to warps that have finished their own (0: none). Share s is then
+    // units 2s (head, its warp) and 2s + 1 (tail, any warp). The unit
+    // boundaries are fixed, so the results do not depend on which warp runs
+    // a tail. tail_ctl (workspace header): [0] next tail, [1] warps finished;
+    // the last warp of the grid to finish sets both back to zero.
+    int tail;
+    unsigned* tail_ctl;
 };
 
 struct MergeArgs {
@@ -416,6 +425,7 @@ struct MergeArgs {
     long long pos_per_warp;
     int contiguous, npv;
     int append;  // fused append: a request with no page is an error (flagged)
+    int tail;  // DecodeArgs::tail of the decode that wrote the partials
 };
 
 // Position range [lo, hi) of request b within one pass over the positions.

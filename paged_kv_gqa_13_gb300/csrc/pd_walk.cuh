@@ -59,6 +59,13 @@ __device__ __forceinline__ size_t kv_row(const DecodeArgs& a, int slab, int kh, 
         return (size_t(slab) * size_t(a.num_kv_heads) + size_t(kh)) * size_t(a.slab_rows) + size_t(row);
 }
 
+// The unit that holds position p: share p / ppw, split into a head and a
+// tail of `tail` positions when tail > 0 (see DecodeArgs::tail).
+__device__ __forceinline__ long long unit_of(long long p, long long ppw, int tail) {
+    const long long sh = p / ppw;
+    return tail ? 2 * sh + ((p - sh * ppw) >= ppw - tail ? 1 : 0) : sh;
+}
+
 // kFused: the decode carries the fused append (DecodeArgs::k_new is set);
 // only then are new-row chunks marked.
 template <bool kFused>
@@ -82,6 +89,19 @@ struct Walk {
         : a(args), s_indptr(si), s_lpl(sl), p0(p0_), pend(pend_), lane(lane_), contiguous(args.contiguous != 0),
           staged(args.table_bytes > 0), wbase(p0_), mask(0), cur(0), j(0), nxt(-1),
           e_slab(0), e_row(0), e_khf(0), e_valid(0), e_qrow(0), e_seg(0) {}
+
+    // Walk a new range [p0_, pend_) (a tail unit): its first page ids are
+    // requested and its first window described.
+    __device__ __forceinline__ void restart(long long p0_, long long pend_) {
+        p0 = p0_;
+        pend = pend_;
+        wbase = p0_;
+        cur = 0;
+        j = 0;
+        const int pg = load_page(p0_ + lane);
+        nxt = load_page(p0_ + 32 + lane);
+        build(p0_, pg);
+    }
 
     // Page id of position p (paged store), -1 outside the range.
     __device__ __forceinline__ int load_page(long long p) const {
