@@ -131,6 +131,18 @@ pd_status allow_smem(const void* fn, int bytes) {
 }
 
 // How a decode call is laid out on the device.
+// Dynamic tails (DecodeArgs::tail): shares of at least kTailMinPos positions
+// give their last 1/kTailDiv, in kTailPieces pieces, to whichever warps
+// finish first. (Measured on GB300: 1/8 in one piece; 1/4 .. 1/6 in two
+// pieces shortened the decode of long batches by ~1% but cost more than
+// that in the merge of the 32-request batch.) The counters sit in the workspace header after the status
+// word. A plan holds 1 + kTailMaxPieces partial slots per warp.
+constexpr long long kTailMinPos = 12;
+constexpr long long kTailDiv = 8;
+constexpr int kTailPieces = 1;
+constexpr int kTailMaxPieces = 1;
+constexpr size_t kTailCtlOff = 64;
+
 struct Plan {
     int group = 0, head_tiles = 0, heads_per_tile = 0, G = 0;
     pd::KernelSet ks{};
@@ -222,7 +234,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->total_warps = (long long)p->ctas * p->nwarps;
     p->segments = (long long)p->head_tiles * Hk * batch;
     p->tails = p->ks.mma == 1;
-    p->slots = (p->tails ? 2 : 1) * p->total_warps + p->segments;
+    p->slots = (p->tails ? 1 + kTailMaxPieces : 1) * p->total_warps + p->segments;
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
     p->ws_bytes = p->o_off + size_t(p->slots) * p->G * D * 4;
@@ -322,13 +334,6 @@ void mark(std::vector<cudaEvent_t>* v, cudaStream_t s) {
 // Test-only: extra bytes warp 0's first pipeline stage waits for (0: off).
 std::atomic<int> g_inject_extra_tx{0};
 
-// Dynamic tails (DecodeArgs::tail): shares of at least kTailMinPos positions
-// give their last 1/kTailDiv to whichever warps finish first. The counters
-// sit in the workspace header after the status word.
-constexpr long long kTailMinPos = 12;
-constexpr long long kTailDiv = 6;
-constexpr size_t kTailCtlOff = 64;
-
 // nhd: the contiguous cache is token-major, [slabs, slab_rows, Hk, D].
 pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, long long slabs, bool nhd,
                         cudaStream_t stream) {
@@ -375,6 +380,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
             // each share is handed out to the warps that finish first.
             if (pl.tails && a.pos_per_warp >= kTailMinPos) {
                 a.tail = int(a.pos_per_warp / kTailDiv);
+                a.tail_pieces = a.tail >= kTailPieces ? kTailPieces : 1;
                 a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
             }
         }
@@ -408,6 +414,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     m.n_pos = a.n_pos;
     m.pos_per_warp = a.pos_per_warp;
     m.tail = a.tail;
+    m.tail_pieces = a.tail_pieces;
     m.contiguous = a.contiguous;
     m.npv = a.npv;
     m.append = (a.k_new != nullptr && !a.contiguous) ? 1 : 0;

@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(256, 1)
     const long long ppw = a.pos_per_warp;
     const long long p0 = gwarp * ppw;
     const long long pend = min(p0 + ppw - a.tail, a.total_pos);  // the head of share gwarp
-    long long unit = a.tail ? 2 * gwarp : gwarp;                   // unit of the chunks being produced
+    const int kp = a.tail_pieces;
+    long long unit = a.tail ? (1 + kp) * gwarp : gwarp;             // unit of the chunks being produced
     bool tails_left = a.tail != 0;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
@@ -122,23 +123,25 @@ __global__ void __launch_bounds__(256, 1)
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(D) * sizeof(T);
-    const long long n_shares = (a.total_pos + ppw - 1) / ppw;
+    const long long n_pieces = a.tail ? (a.total_pos + ppw - 1) / ppw * kp : 0;
+    const long long piece = a.tail ? a.tail / kp : 0;
     auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
         bool have = walk.template next<kMmaRows>(&ck);
-        // This warp's range is done: take the next share's tail, if any is left.
+        // This warp's range is done: take the next tail piece, if any is left.
         while (!have && tails_left) {
             unsigned t = 0;
             if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
             t = __shfl_sync(kFull, t, 0);
-            if ((long long)t >= n_shares) {
+            if ((long long)t >= n_pieces) {
                 tails_left = false;
                 break;
             }
-            const long long t0 = (long long)t * ppw + (ppw - a.tail);
-            const long long t1 = min(t0 + a.tail, a.total_pos);
+            const long long sh = (long long)t / kp, jp = (long long)t % kp;
+            const long long t0 = sh * ppw + (ppw - a.tail) + jp * piece;
+            const long long t1 = min(jp == kp - 1 ? (sh + 1) * ppw : t0 + piece, a.total_pos);
             if (t0 >= t1) continue;
-            unit = 2 * (long long)t + 1;
+            unit = (1 + kp) * sh + 1 + jp;
             walk.restart(t0, t1);
             have = walk.template next<kMmaRows>(&ck);
         }

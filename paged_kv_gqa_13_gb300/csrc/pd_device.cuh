@@ -403,13 +403,16 @@ struct DecodeArgs {
     // of every pass (token-major contiguous cache).
     int unit_transpose;
     // Positions at the end of each warp's share (pos_per_warp) that its warp
-    // does not run: they form one more unit per share, handed out in share
-    // order to warps that have finished their own (0: none). Share s is then
-    // units 2s (head, its warp) and 2s + 1 (tail, any warp). The unit
-    // boundaries are fixed, so the results do not depend on which warp runs
-    // a tail. tail_ctl (workspace header): [0] next tail, [1] warps finished;
-    // the last warp of the grid to finish sets both back to zero.
+    // does not run (0: none): they are cut into tail_pieces units (the last
+    // takes the remainder), handed out in share order to warps that have
+    // finished their own range. Share s is units (1 + k) s (head, its warp)
+    // and (1 + k) s + 1 .. (1 + k) s + k (tail pieces, any warp), k =
+    // tail_pieces. The unit boundaries are fixed, so the results do not
+    // depend on which warp runs a piece. tail_ctl (workspace header): [0]
+    // next piece, [1] warps finished; the last warp of the grid to finish
+    // sets both back to zero.
     int tail;
+    int tail_pieces;
     unsigned* tail_ctl;
 };
 
@@ -425,7 +428,7 @@ struct MergeArgs {
     long long pos_per_warp;
     int contiguous, npv;
     int append;  // fused append: a request with no page is an error (flagged)
-    int tail;  // DecodeArgs::tail of the decode that wrote the partials
+    int tail, tail_pieces;  // DecodeArgs::tail, tail_pieces of the decode that wrote the partials
 };
 
 // Position range [lo, hi) of request b within one pass over the positions.

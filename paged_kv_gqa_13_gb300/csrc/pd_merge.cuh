@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs 
     float L = kNegInf;
     if (a.append && hi <= lo && sh == 0 && h == 0 && lane == 0) atomicOr(a.flags, kFlagBadIndptr);
     if (hi > lo) {
-        const long long first = unit_of((long long)sh * a.n_pos + lo, a.pos_per_warp, a.tail);
-        const long long last = unit_of((long long)sh * a.n_pos + hi - 1, a.pos_per_warp, a.tail);
+        const long long first = unit_of((long long)sh * a.n_pos + lo, a.pos_per_warp, a.tail, a.tail_pieces);
+        const long long last = unit_of((long long)sh * a.n_pos + hi - 1, a.pos_per_warp, a.tail, a.tail_pieces);
         if (first == last) return;  // one warp held the whole request and wrote it
         grid_dependency_wait();     // the decode kernel's partials are complete and visible
         const int parts = int(last - first + 1);

@@ -59,11 +59,16 @@ __device__ __forceinline__ size_t kv_row(const DecodeArgs& a, int slab, int kh, 
         return (size_t(slab) * size_t(a.num_kv_heads) + size_t(kh)) * size_t(a.slab_rows) + size_t(row);
 }
 
-// The unit that holds position p: share p / ppw, split into a head and a
-// tail of `tail` positions when tail > 0 (see DecodeArgs::tail).
-__device__ __forceinline__ long long unit_of(long long p, long long ppw, int tail) {
+// The unit that holds position p: share p / ppw, split into a head and
+// `pieces` tail pieces of tail / pieces positions (the last one takes the
+// remainder) when tail > 0 (see DecodeArgs::tail).
+__device__ __forceinline__ long long unit_of(long long p, long long ppw, int tail, int pieces) {
     const long long sh = p / ppw;
-    return tail ? 2 * sh + ((p - sh * ppw) >= ppw - tail ? 1 : 0) : sh;
+    if (tail == 0) return sh;
+    const long long r = p - sh * ppw, head = ppw - tail;
+    if (r < head) return (1 + pieces) * sh;
+    const long long j = min((r - head) / (tail / pieces), (long long)pieces - 1);
+    return (1 + pieces) * sh + 1 + j;
 }
 
 // kFused: the decode carries the fused append (DecodeArgs::k_new is set);

@@ -1,5 +1,5 @@
 """Dynamic share tails of the tensor-core decode: shapes with enough positions
-per warp that the last sixth of each warp's share is handed out at run time to
+per warp that the last eighth of each warp's share is handed out at run time to
 the warps that finish first. The unit boundaries are fixed, so the results must
 not depend on which warp ran which tail, and the tail counters in the workspace
 header must be back at zero after every call."""
