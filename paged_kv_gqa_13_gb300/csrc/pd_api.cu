@@ -146,7 +146,7 @@ constexpr size_t kTailCtlOff = 64;
 struct Plan {
     int group = 0, head_tiles = 0, heads_per_tile = 0, G = 0;
     pd::KernelSet ks{};
-    int table_bytes = 0, nwarps = 0, ctas = 0;
+    int table_bytes = 0, nwarps = 0, ctas = 0, sms = 0;
     long long total_warps = 0, segments = 0, slots = 0;
     bool tails = false;  // the decode kernel takes DecodeArgs::tail (slots for two units per warp)
     size_t smem = 0, lse_off = 0, o_off = 0, ws_bytes = 0;
@@ -231,6 +231,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     }
     if (per_sm < 1) per_sm = 1;
     p->ctas = di.sms * per_sm;
+    p->sms = di.sms;
     p->total_warps = (long long)p->ctas * p->nwarps;
     p->segments = (long long)p->head_tiles * Hk * batch;
     p->tails = p->ks.mma == 1;
@@ -430,7 +431,9 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     cfg.numAttrs = 1;
     void* margs[] = {&m};
     if (prof) mark(&g_prof.merge_marks, stream);
-    e = cudaLaunchKernelExC(&cfg, pl.ks.merge, margs);
+    // one wave of 4-warp blocks at 4 per SM: the wide merge (fewer round trips)
+    const void* mk = pairs <= (long long)pl.sms * 16 ? pl.ks.merge_wide : pl.ks.merge;
+    e = cudaLaunchKernelExC(&cfg, mk, margs);
     if (prof) mark(&g_prof.merge_marks, stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     return ok();

@@ -15,6 +15,7 @@ struct KernelSet {
     const void* decode;
     const void* variant[4];  // decode kernel per variant bits (variant[0] == decode)
     const void* merge;
+    const void* merge_wide;  // the merge with rounds of twice the parts, for grids of one wave at 4 blocks per SM
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
     int rows_per_stage;  // K (and V) rows one pipeline stage holds
@@ -53,6 +54,7 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
         ks->merge = reinterpret_cast<const void*>(merge_partials_kernel<T, DD>);        \
+        ks->merge_wide = reinterpret_cast<const void*>(merge_partials_kernel<T, DD, true>); \
         ks->merge_states = reinterpret_cast<const void*>(merge_states_kernel<T, DD>);   \
         if constexpr (kHalf && GG >= 4) {                                               \
             PD_MMA(DD)                                                                  \

@@ -80,12 +80,14 @@ __device__ __forceinline__ void store_row(T* orow, const float* acc) {
 // order; write zeros / -inf for requests with no pages. Everything that does
 // not depend on the decode's output (the page table, empty requests) is done
 // before waiting for the decode grid.
-template <typename T, int D>
-// Its grid follows the decode with one warp per (segment, head); registers
+// Its grid follows the decode with one warp per (segment, head). Registers
 // are held to 85 per thread (rounds of 8 parts, 4 at head_dim 256) so that 6
 // blocks fit per SM and the warps that remain after the decode run in few
-// waves.
-__global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs a) {
+// waves. kWide (for grids that fit one wave at 4 blocks per SM): rounds of 16
+// parts (8 at 256), so that requests split over up to 16 units take one
+// round trip.
+template <typename T, int D, bool kWide = false>
+__global__ void __launch_bounds__(128, kWide ? 4 : 6) merge_partials_kernel(const MergeArgs a) {
     constexpr int kPer = D / 32;  // elements per lane
     const float kNegInf = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31;
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(128, 6) merge_partials_kernel(const MergeArgs 
         grid_dependency_wait();     // the decode kernel's partials are complete and visible
         const int parts = int(last - first + 1);
         const long long slot0 = (first + s) * a.G + h;  // slot of part c: (first + c + s) * G + h
-        L = merge_rows<kPer, (D <= 128 ? 8 : 4)>(
+        L = merge_rows<kPer, (D <= 128 ? 8 : 4) * (kWide ? 2 : 1)>(
             parts, [&](int cp) { return a.part_lse[slot0 + (long long)cp * a.G]; },
             [&](int cp) { return a.part_o + size_t(slot0 + (long long)cp * a.G) * D; }, acc);
     }
