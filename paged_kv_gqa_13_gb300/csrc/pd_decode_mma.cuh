@@ -98,8 +98,7 @@ __global__ void __launch_bounds__(256, 1)
     const long long ppw = a.pos_per_warp;
     const long long p0 = gwarp * ppw;
     const long long pend = min(p0 + ppw - a.tail, a.total_pos);  // the head of share gwarp
-    const int kp = a.tail_pieces;
-    long long unit = a.tail ? (1 + kp) * gwarp : gwarp;             // unit of the chunks being produced
+    long long unit = a.tail ? (1 + a.tail_pieces) * gwarp : gwarp;  // unit of the chunks being produced
     bool tails_left = a.tail != 0;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
@@ -123,27 +122,13 @@ __global__ void __launch_bounds__(256, 1)
 
     const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(D) * sizeof(T);
-    const long long n_pieces = a.tail ? (a.total_pos + ppw - 1) / ppw * kp : 0;
-    const long long piece = a.tail ? a.tail / kp : 0;
     auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
         bool have = walk.template next<kMmaRows>(&ck);
         // This warp's range is done: take the next tail piece, if any is left.
         while (!have && tails_left) {
-            unsigned t = 0;
-            if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
-            t = __shfl_sync(kFull, t, 0);
-            if ((long long)t >= n_pieces) {
-                tails_left = false;
-                break;
-            }
-            const long long sh = (long long)t / kp, jp = (long long)t % kp;
-            const long long t0 = sh * ppw + (ppw - a.tail) + jp * piece;
-            const long long t1 = min(jp == kp - 1 ? (sh + 1) * ppw : t0 + piece, a.total_pos);
-            if (t0 >= t1) continue;
-            unit = (1 + kp) * sh + 1 + jp;
-            walk.restart(t0, t1);
-            have = walk.template next<kMmaRows>(&ck);
+            tails_left = take_tail(a, walk, &unit, lane);
+            if (tails_left) have = walk.template next<kMmaRows>(&ck);
         }
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
@@ -360,18 +345,7 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
         produce(slot, 0u);
     }
-    if (a.tail != 0 && lane == 0) {
-        // Every warp of the grid passes here once; the last one resets the
-        // tail counters for the next call (no grab can follow: every warp
-        // has stopped taking tails before it counts itself finished).
-        __threadfence();
-        const unsigned warps = gridDim.x * unsigned(nwarps);
-        if (atomicAdd(a.tail_ctl + 1, 1u) == warps - 1u) {
-            __threadfence();
-            atomicExch(a.tail_ctl, 0u);
-            atomicExch(a.tail_ctl + 1, 0u);
-        }
-    }
+    tails_finished(a, nwarps, lane);
 }
 
 }  // namespace pd

@@ -302,6 +302,44 @@ struct Walk {
     }
 };
 
+// Dynamic tails (DecodeArgs::tail). Point `walk` at the next tail piece not
+// yet taken and set *unit to its unit; false when none is left. Called by the
+// whole warp.
+template <class W>
+__device__ __forceinline__ bool take_tail(const DecodeArgs& a, W& walk, long long* unit, int lane) {
+    const long long ppw = a.pos_per_warp;
+    const int kp = a.tail_pieces;
+    const long long n_pieces = (a.total_pos + ppw - 1) / ppw * kp;
+    const long long piece = a.tail / kp;
+    for (;;) {
+        unsigned t = 0;
+        if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
+        t = __shfl_sync(kFull, t, 0);
+        if ((long long)t >= n_pieces) return false;
+        const long long sh = (long long)t / kp, jp = (long long)t % kp;
+        const long long t0 = sh * ppw + (ppw - a.tail) + jp * piece;
+        const long long t1 = min(jp == kp - 1 ? (sh + 1) * ppw : t0 + piece, a.total_pos);
+        if (t0 >= t1) continue;  // past the last position
+        *unit = (1 + kp) * sh + 1 + jp;
+        walk.restart(t0, t1);
+        return true;
+    }
+}
+
+// Every warp of a grid with tails calls this once, after its last chunk; the
+// last one resets the tail counters for the next call (no warp takes a piece
+// after it has counted itself finished).
+__device__ __forceinline__ void tails_finished(const DecodeArgs& a, int nwarps, int lane) {
+    if (a.tail == 0 || lane != 0) return;
+    __threadfence();
+    const unsigned warps = gridDim.x * unsigned(nwarps);
+    if (atomicAdd(a.tail_ctl + 1, 1u) == warps - 1u) {
+        __threadfence();
+        atomicExch(a.tail_ctl, 0u);
+        atomicExch(a.tail_ctl + 1, 0u);
+    }
+}
+
 // Fused append: the whole warp writes request b's new K and V rows for kv
 // head ck.kh into the chunk's last row (row ck.row0 + ck.rows - 1 of its
 // slab), then fences them so that the chunk's copy, issued afterwards by
