@@ -22,7 +22,7 @@ def _raw(t, dtype):
 
 
 @pytest.mark.parametrize("dtype,Hq,Hk,D,L,valid", [
-    ("f16", 32, 8, 128, 5000, 4999),   # group 4, CUDA cores, split across warps
+    ("f16", 32, 8, 128, 5000, 4999),   # group 4, tensor cores, per-token-range units
     ("bf16", 64, 8, 128, 777, 700),    # group 8, tensor cores
     ("bf16", 16, 2, 256, 300, 291),    # group 8, D 256, tensor cores
     ("f32", 8, 8, 64, 100, 100),       # MHA f32

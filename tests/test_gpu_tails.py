@@ -41,3 +41,39 @@ def test_tails_repeatable_and_match_oracle(make):
         assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse, l1)
     assert _counters(dw.ws) == [0, 0]
     compare(o1, l1, *oracle.paged_decode_workload(w), w.dtype, "tails")
+
+
+def test_tails_on_the_token_major_cache():
+    """NHD contiguous cache with 8 kv heads (the per-token-range unit layout),
+    ~50 positions per warp: tails taken at run time, results repeatable bit for
+    bit and equal to the oracle's."""
+    import math
+
+    import numpy as np
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+    from tests.gpu_helpers import to_dev
+
+    B, L, valid, Hq, Hk, D, dtype = 3, 40000, 39990, 32, 8, 128, "f16"
+    seed = 75
+    kc = wl.normal((B, L, Hk, D), dtype, wl.stream_key(seed, "k"))
+    vc = wl.normal((B, L, Hk, D), dtype, wl.stream_key(seed, "v"))
+    q = wl.normal((B, Hq, D), dtype, wl.stream_key(seed, "q"))
+    kc[:, valid:] = wl.nan_value(dtype)
+    vc[:, valid:] = wl.nan_value(dtype)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    qd, kd, vd = to_dev(q, dtype), to_dev(kc, dtype), to_dev(vc, dtype)
+    ws = pd.alloc_workspace(pd.pd_contiguous_decode_workspace_bytes(B, Hq, Hk, D, pd.PD_F16))
+    o1 = torch.empty_like(qd)
+    l1 = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    pd.pd_contiguous_decode_nhd(qd, kd, vd, o1, l1, valid, scale, ws)
+    assert pd.pd_read_device_flags(ws) == 0
+    for _ in range(3):
+        o = torch.empty_like(qd)
+        lse = torch.empty_like(l1)
+        pd.pd_contiguous_decode_nhd(qd, kd, vd, o, lse, valid, scale, ws)
+        assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse, l1)
+    assert _counters(ws) == [0, 0]
+    o_ref, lse_ref = oracle.contiguous_decode(q, kc, vc, Hq, valid, scale, dtype, layout="nhd")
+    compare(o1, l1, o_ref, lse_ref, dtype, "nhd with tails")
