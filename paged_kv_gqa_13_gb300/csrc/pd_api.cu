@@ -234,9 +234,9 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->sms = di.sms;
     p->total_warps = (long long)p->ctas * p->nwarps;
     p->segments = (long long)p->head_tiles * Hk * batch;
-    // The 16-bit tensor-core kernel. (The E4M3 kernel's two-stage ring cannot
-    // hide a tail's start: measured 36 -> 43 us on the Llama-shaped batch.)
-    p->tails = p->ks.mma == 1;
+    // All but the E4M3 tensor-core kernel, whose two-stage ring cannot hide a
+    // tail's start (measured 36 -> 43 us on the Llama-shaped batch).
+    p->tails = p->ks.mma != 2;
     p->slots = (p->tails ? 1 + kTailMaxPieces : 1) * p->total_warps + p->segments;
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;

@@ -10,8 +10,8 @@
 // long request is split over several warps (split-KV), many short ones share
 // a warp. Where a warp's range covers a request's whole page list the warp
 // writes o and lse itself; otherwise it writes a normalised partial (o, lse)
-// into workspace slot (warp + segment), and merge_partials_kernel combines
-// the partials in warp order.
+// into workspace slot (unit + segment), and merge_partials_kernel combines
+// the partials in unit order.
 //
 // Inside a warp. The warp runs its own kStages-deep ring in shared memory.
 // Lane 0 issues 1-D bulk async copies (cp.async.bulk) of K and V page slices
@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(256, 1)
     const long long gwarp = a.unit_transpose ? (long long)wid * gridDim.x + blockIdx.x
                                              : (long long)blockIdx.x * nwarps + wid;
     const long long p0 = gwarp * a.pos_per_warp;
-    const long long pend = min(p0 + a.pos_per_warp, a.total_pos);
+    const long long pend = min(p0 + a.pos_per_warp - a.tail, a.total_pos);  // the head of share gwarp
+    long long unit = a.tail ? (1 + a.tail_pieces) * gwarp : gwarp;           // unit of the chunks produced
+    bool tails_left = a.tail != 0;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256, 1)
     // Let the merge kernel be scheduled now; it waits for this grid before it
     // reads any partial result.
     launch_dependents();
-    if (p0 >= pend) return;
+    if (p0 >= pend && !tails_left) return;  // with tails a warp without a head may still take some
     walk.build(p0, first_page);
 
     const uint64_t policy = l2_evict_first_policy();
@@ -141,7 +143,12 @@ __global__ void __launch_bounds__(256, 1)
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
-        const bool have = walk.template next<kRC>(&ck);
+        bool have = walk.template next<kRC>(&ck);
+        // This warp's range is done: take the next tail piece, if any is left.
+        while (!have && tails_left) {
+            tails_left = take_tail(a, walk, &unit, lane);
+            if (tails_left) have = walk.template next<kRC>(&ck);
+        }
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
         if constexpr (kFused) {
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar);
             return;
         }
-        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg);
+        meta[slot] = make_int4(ck.rows, ck.flags, ck.qrow, ck.seg + int(unit));  // .w: partial slot
         // An NHD box lands whole: kRC rows, those past the valid length as zeros.
         const uint32_t kv_bytes =
             kNhd ? (ck.rows > 0 ? uint32_t(kChunkBytes) : 0u) : uint32_t(ck.rows) * uint32_t(kv_row_bytes);
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(256, 1)
         RSR::run(flat, lane);
         const int qrow = m.z;  // first q / o row of the group
         const bool complete = (m.y & kSegComplete) != 0;
-        const long long slot = gwarp + m.w;
+        const long long slot = m.w;
 #pragma unroll
         for (int j = 0; j < kOwn; ++j) {
             const int x = RSR::index(j, lane);
@@ -427,6 +434,7 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
         produce(slot, 0u);
     }
+    tails_finished(a, nwarps, lane);
 }
 
 

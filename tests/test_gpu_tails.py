@@ -1,4 +1,4 @@
-"""Dynamic share tails of the tensor-core decode: shapes with enough positions
+"""Dynamic share tails of the decode kernels: shapes with enough positions
 per warp that the last eighth of each warp's share is handed out at run time to
 the warps that finish first. The unit boundaries are fixed, so the results must
 not depend on which warp ran which tail, and the tail counters in the workspace
@@ -27,6 +27,8 @@ def _counters(ws):
     lambda: wl.make_paged("tails_f16_g8", "f16", [20000, 1, 8000, 17, 24000, 600], 64, 8, 128, 16, seed=72),
     # one-row pages at head_dim 64: ~50 positions per warp, segments of over 32 parts
     lambda: wl.make_paged("tails_bf16_d64_p1", "bf16", [3000, 5000, 1], 32, 8, 64, 1, seed=73),
+    # f32 MHA on the CUDA-core kernel, ~16 positions per warp
+    lambda: wl.make_paged("tails_f32_mha", "f32", [12000, 1, 9000, 17, 10000], 8, 8, 128, 16, seed=76),
 ])
 def test_tails_repeatable_and_match_oracle(make):
     import torch
@@ -38,7 +40,8 @@ def test_tails_repeatable_and_match_oracle(make):
     assert _counters(dw.ws) == [0, 0]
     for _ in range(3):
         o, lse = dw.decode()
-        assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse, l1)
+        assert torch.equal(o, o1) if w.dtype == "f32" else torch.equal(o.view(torch.int16), o1.view(torch.int16))
+        assert torch.equal(lse, l1)
     assert _counters(dw.ws) == [0, 0]
     compare(o1, l1, *oracle.paged_decode_workload(w), w.dtype, "tails")
 
