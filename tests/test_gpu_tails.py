@@ -80,3 +80,45 @@ def test_tails_on_the_token_major_cache():
     assert _counters(ws) == [0, 0]
     o_ref, lse_ref = oracle.contiguous_decode(q, kc, vc, Hq, valid, scale, dtype, layout="nhd")
     compare(o1, l1, o_ref, lse_ref, dtype, "nhd with tails")
+
+
+@pytest.mark.parametrize("dtype,Hq,Hk,D,lens", [
+    ("bf16", 32, 8, 128, [20000, 0, 15, 9000, 16000, 1]),   # tensor cores, ~19 positions per warp
+    ("f16", 16, 16, 256, [12000, 1, 7000]),                 # CUDA cores (MHA), ~16 positions per warp
+])
+def test_tails_with_the_fused_append(dtype, Hq, Hk, D, lens):
+    """Fused append + decode on shapes that take tails: the pool ends bit for
+    bit as the oracle's append leaves it, o and lse are bit-identical to the
+    append launch followed by the decode, and they match the oracle."""
+    import numpy as np
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+    from tests.gpu_helpers import to_dev, to_host_raw
+
+    steps = 2
+    w = wl.make_paged(f"tails_fused_{dtype}_{Hq}_{Hk}", dtype, lens, Hq, Hk, D, 16, seed=77 + Hq,
+                      extra_rows=steps, append_steps=steps)
+    fused, split = DeviceWorkload(w), DeviceWorkload(w)
+    k_host, v_host = w.k_data.copy(), w.v_data.copy()
+    t = w.table
+    for step in range(steps):
+        t = wl.table_after_append(t)
+        kn, vn = w.new_rows(step)
+        knd, vnd = to_dev(kn, dtype), to_dev(vn, dtype)
+        fused.set_table(t)
+        split.set_table(t)
+        pd.pd_paged_append_decode(fused.q, knd, vnd, fused.k, fused.v, fused.indices, fused.indptr, fused.lpl,
+                                  fused.o, fused.lse, w.sm_scale, fused.ws)
+        pd.pd_paged_append(knd, vnd, split.k, split.v, split.indices, split.indptr, split.lpl, split.ws)
+        o2, l2 = split.decode()
+        oracle.paged_append(kn, vn, k_host, v_host, t.indices, t.indptr, t.last_page_len, dtype)
+        assert np.array_equal(to_host_raw(fused.k, dtype).view(np.uint16), k_host.view(np.uint16))
+        assert np.array_equal(to_host_raw(fused.v, dtype).view(np.uint16), v_host.view(np.uint16))
+        assert torch.equal(fused.o.view(torch.int16), o2.view(torch.int16)) and torch.equal(fused.lse, l2)
+        assert fused.flags() == 0 and split.flags() == 0
+        assert _counters(fused.ws) == [0, 0] and _counters(split.ws) == [0, 0]
+        o_ref, lse_ref = oracle.paged_decode(w.q, k_host, v_host, t.indices, t.indptr, t.last_page_len,
+                                             w.num_qo_heads, w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale,
+                                             dtype)
+        compare(fused.o, fused.lse, o_ref, lse_ref, dtype, f"fused with tails, step {step}")
