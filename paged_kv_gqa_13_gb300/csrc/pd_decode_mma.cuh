@@ -108,21 +108,49 @@ __global__ void __launch_bounds__(256, 1)
         prefetch_tensormap(&tmv);
     }
 
+    const uint64_t policy = l2_evict_first_policy();
+    // Paged pools of pages of at most 16 rows, without the fused append: chunk
+    // s of this warp is position p0 + s, so the first stages' copies go out as
+    // soon as their page ids are known, before the table is staged (they take
+    // the place of the first-slab L2 prefetch). A bad page id is an
+    // out-of-range coordinate, which reads zeros; its chunk has no rows.
+    const int n_early = (!kFused && !kNhd && !a.contiguous && a.page_size <= kMmaRows)
+                            ? int(min((long long)kS, max(pend - p0, 0LL)))
+                            : 0;
     walk.stage_table(s_indptr, s_lpl, [&] {
         if (lane == 0) {
             for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
         }
-        walk.template prefetch_first_slabs<kNhd>(first_page, kS, size_t(D) * sizeof(T));
+        if (n_early == 0) {
+            walk.template prefetch_first_slabs<kNhd>(first_page, kS, size_t(D) * sizeof(T));
+            return;
+        }
+        for (int s = 0; s < n_early; ++s) {
+            const int pg = __shfl_sync(kFull, first_page, s);
+            if (lane == 0) {
+                const int kh = int((p0 + s) / a.n_pos) / a.head_tiles;
+                const uint32_t bar = bar0 + 8 * s;
+                const uint32_t st = wsm_u32 + s * C::kStageBytes;
+                // a.test_extra_tx (test-only, normally 0): see the first produce calls below
+                mbar_arrive_expect_tx(bar, 2u * C::kKBytes + ((s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u));
+#pragma unroll
+                for (int bx = 0; bx < C::kBoxes; ++bx) {
+                    tma_load_4d(st + bx * C::kBoxBytes, &tmk, bx * 64, 0, kh, pg, bar, policy);
+                    tma_load_4d(st + C::kKBytes + bx * C::kBoxBytes, &tmv, bx * 64, 0, kh, pg, bar, policy);
+                }
+            }
+        }
     });
     __syncthreads();  // the only block-wide barrier
     launch_dependents();
     if (p0 >= pend && !tails_left) return;  // with tails a warp without a head may still take some
     walk.build(p0, first_page);
 
-    const uint64_t policy = l2_evict_first_policy();
     const size_t row_bytes = size_t(D) * sizeof(T);
-    auto produce = [&](int slot, uint32_t extra_tx) {
+    // issued: the chunk's copies went out early (see n_early); only its
+    // description is written here.
+    auto produce = [&](int slot, uint32_t extra_tx, bool issued) {
         Chunk ck;
         bool have = walk.template next<kMmaRows>(&ck);
         // This warp's range is done: take the next tail piece, if any is left.
@@ -148,6 +176,7 @@ __global__ void __launch_bounds__(256, 1)
         // consumer reads them from there when it reaches that chunk.
         if (ck.flags & kSegStart)
             bulk_prefetch_l2(static_cast<const uint8_t*>(a.q) + size_t(ck.qrow) * row_bytes, uint32_t(GT * row_bytes));
+        if (issued) return;
         const uint32_t total = 2 * kv_bytes;
         if (total == 0) {
             mbar_arrive(bar);
@@ -326,7 +355,7 @@ __global__ void __launch_bounds__(256, 1)
     // a.test_extra_tx (test-only, normally 0): warp 0's first stage expects
     // bytes that never arrive, so that its bounded wait runs out.
 #pragma unroll 1
-    for (int s = 0; s < kS; ++s) produce(s, (s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u);
+    for (int s = 0; s < kS; ++s) produce(s, (s == 0 && gwarp == 0) ? uint32_t(a.test_extra_tx) : 0u, s < n_early);
 #pragma unroll 1
     for (int it = 0;; ++it) {
         const int slot = it % kS;
@@ -343,7 +372,7 @@ __global__ void __launch_bounds__(256, 1)
         if (m.y & kEndOfWork) break;
         consume(slot, m);
         __syncwarp();
-        produce(slot, 0u);
+        produce(slot, 0u, false);
     }
     tails_finished(a, nwarps, lane);
 }
