@@ -92,7 +92,10 @@ size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_h
  * Batched paged decode (batch_paged_decode.rs: BatchPagedDecodePlan::run and
  * the per-dtype FFI launch it makes, whose argument order this follows).
  *
- * q, k_data, v_data, o: device, 16-byte aligned, layouts above.
+ * q, k_data, v_data, o: device, 16-byte aligned, layouts above. o (and lse)
+ *   may also be pinned host memory (cudaHostAlloc / cudaMallocHost), which
+ *   kernels reach at its host address under unified addressing: the kernels
+ *   then store the results straight into host memory, with no copy back.
  * indices (may be NULL only if num_indices == 0), indptr, last_page_len: device int32.
  * lse: device float32 [batch, num_qo_heads], natural log.
  * head_dim: 64, 128 or 256. num_qo_heads % num_kv_heads == 0.

@@ -1,7 +1,7 @@
 """GPU parity for paths the workload shapes do not reach: a batch above the
 staged page-table size, the contiguous entry on the tensor-core kernel, a long
 request split across many units on the tensor-core kernel, and the decode
-captured into a CUDA graph and replayed."""
+captured into a CUDA graph and replayed, and outputs in pinned host memory."""
 import math
 
 import numpy as np
@@ -84,3 +84,22 @@ def test_decode_replays_from_a_cuda_graph(make):
     torch.cuda.synchronize()
     w.q = q2
     compare(dw.o, dw.lse, *oracle.paged_decode_workload(w), w.dtype, "graph replay, new q")
+
+
+def test_outputs_in_pinned_host_memory():
+    """o and lse may be pinned host memory: the decode and merge kernels store
+    the results there directly, bit-identical to a device-resident decode."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.llama3_8b_bf16(seed=95, batch=12, lo=1, hi=3000)  # split requests: merged rows and direct rows
+    dw = DeviceWorkload(w)
+    o_dev, l_dev = [t.clone() for t in dw.decode()]
+    oh = torch.empty(o_dev.shape, dtype=o_dev.dtype).pin_memory()
+    lh = torch.empty(l_dev.shape, dtype=torch.float32).pin_memory()
+    pd.pd_paged_decode(dw.q, dw.k, dw.v, dw.indices, dw.indptr, dw.lpl, oh, lh, w.sm_scale, dw.ws)
+    torch.cuda.synchronize()
+    assert dw.flags() == 0
+    assert torch.equal(oh.view(torch.int16), o_dev.cpu().view(torch.int16))
+    assert torch.equal(lh, l_dev.cpu())
