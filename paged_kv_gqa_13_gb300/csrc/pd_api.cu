@@ -374,23 +374,18 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
             a.total_pos = passes * a.n_pos;
             a.unit_transpose = 1;
             grid = int(w);
-            if (pl.tails && a.pos_per_warp >= kTailMinPos) {
-                a.tail = int(a.pos_per_warp / kTailDiv);
-                a.tail_pieces = a.tail >= kTailPieces ? kTailPieces : 1;
-                a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
-            }
         } else {
             a.pos_per_warp = (a.total_pos + pl.total_warps - 1) / pl.total_warps;
             const long long warps_used = (a.total_pos + a.pos_per_warp - 1) / a.pos_per_warp;
             grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
-            // SMs stream at different rates (by up to ~25% across one GPU), so
-            // equal shares end at different times: the last kTailDiv-th of
-            // each share is handed out to the warps that finish first.
-            if (pl.tails && a.pos_per_warp >= kTailMinPos) {
-                a.tail = int(a.pos_per_warp / kTailDiv);
-                a.tail_pieces = a.tail >= kTailPieces ? kTailPieces : 1;
-                a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
-            }
+        }
+        // SMs stream at different rates (by up to ~25% across one GPU), so
+        // equal shares end at different times: the last kTailDiv-th of each
+        // share is handed out to the warps that finish first.
+        if (pl.tails && a.pos_per_warp >= kTailMinPos) {
+            a.tail = int(a.pos_per_warp / kTailDiv);
+            a.tail_pieces = a.tail >= kTailPieces ? kTailPieces : 1;
+            a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
         }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
