@@ -120,3 +120,23 @@ def test_fp8_append_saturates_and_rounds_ties_to_even():
                            dev.ptr, dev.lpl, dev.ws)
     oracle.paged_append_fp8(kn, vn, dev.ks, dev.vs, dev.k8, dev.v8, t.indices, t.indptr, t.last_page_len, "f16")
     assert np.array_equal(dev.k.cpu().numpy(), dev.k8) and np.array_equal(dev.v.cpu().numpy(), dev.v8)
+
+
+def test_fp8_cuda_core_kernel_with_share_tails():
+    """E4M3 pool at group 2 (the CUDA-core kernel) with ~15 positions per warp,
+    so that share tails are handed out: repeated calls agree bit for bit, the
+    tail counters (workspace header bytes 64..71) return to zero, and the result
+    matches the oracle."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("fp8_tails_g2", "f16", [16000, 1, 9000, 17, 8000], 16, 8, 128, 16, seed=78)
+    dev = Fp8Device(w)
+    o1, l1 = [t.clone() for t in dev.decode()]
+    assert pd.pd_read_device_flags(dev.ws) == 0
+    for _ in range(3):
+        o, lse = dev.decode()
+        assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse, l1)
+    assert dev.ws[64:72].view(torch.int32).cpu().tolist() == [0, 0]
+    compare(o1, l1, *dev.oracle_decode(), w.dtype, "fp8 CUDA-core decode with share tails")
