@@ -84,7 +84,8 @@ def test_nhd_zero_valid_rows():
 
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("dtype,Hq,Hk,D,L", [("f16", 32, 8, 128, 300), ("bf16", 64, 8, 128, 97),
-                                             ("f32", 8, 8, 64, 40), ("bf16", 16, 4, 256, 65)])
+                                             ("f32", 8, 8, 64, 40), ("bf16", 16, 4, 256, 65),
+                                             ("f16", 32, 8, 128, 40000)])  # ~50 positions per warp: share tails
 def test_nhd_append_then_decode(dtype, Hq, Hk, D, L, fused):
     import torch
 
