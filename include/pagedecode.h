@@ -108,8 +108,10 @@ size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_h
  *   be ordered on one stream.
  *
  * Long requests are split across warps in a load-balanced partition of all
- * (kv head, page) work; partial (o, lse) pairs are combined by a merge
- * kernel in a fixed order, so results do not depend on timing.
+ * (kv head, page) work; the last eighth of each warp's share goes, at fixed
+ * boundaries, to whichever warp finishes first (counters in the workspace
+ * header, back at zero after every call). Partial (o, lse) pairs are combined
+ * by a merge kernel in a fixed order, so results do not depend on timing.
  */
 pd_status pd_paged_decode(const void* q, const void* k_data, const void* v_data,
                           const int32_t* indices, const int32_t* indptr,
