@@ -275,7 +275,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         flush_w.zero_()
         flush_r.sum()
 
-    # in-process copy-kernel bandwidth (reported beside the driver's measured peak)
+    # in-process copy-kernel bandwidth (reported beside the measured peak of MEASURED_PEAKS.json)
     copy_gbs = None
     if not args.quick:
         src = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
