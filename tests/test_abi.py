@@ -92,3 +92,36 @@ def test_contiguous_and_append_and_merge_reject_bad_arguments():
     assert L.pd_merge_states(FAKE, FAKE, 2, 4, 100, FAKE, None, pd.PD_F32, None) == pd.PD_ERR_UNSUPPORTED
     assert L.pd_copy_bytes(FAKE, FAKE, 10, None) == pd.PD_ERR_UNSUPPORTED
     assert L.pd_workspace_init(FAKE, 8, None) == pd.PD_ERR_WORKSPACE
+
+
+def test_a_c_program_compiles_links_and_runs_against_the_header(tmp_path):
+    """The boundary is usable from plain C: a C11 translation unit includes the
+    header, takes the address of every declared entry point, links against the
+    built library and calls the two entry points that need no device."""
+    import shutil
+    import subprocess
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = _declared()
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "pagedecode.h"\n'
+        "int main(void) {\n"
+        "    void (*fns[])(void) = {" + ", ".join(f"(void (*)(void)){n}" for n in names) + "};\n"
+        "    int nonnull = 0;\n"
+        "    for (unsigned i = 0; i < sizeof fns / sizeof fns[0]; ++i) nonnull += fns[i] != 0;\n"
+        "    printf(\"%d %d %s\\n\", nonnull, pd_version(), pd_last_error_string() ? \"str\" : \"null\");\n"
+        "    return 0;\n}\n")
+    libdir = os.path.dirname(pd.LIBRARY_PATH)
+    exe = tmp_path / "use_abi"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-lpagedecode", f"-Wl,-rpath,{libdir}",
+                    "-Wl,--unresolved-symbols=ignore-in-shared-libs", "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    env = dict(os.environ)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, env=env).stdout.split()
+    assert out == [str(len(names)), "1", "str"]
