@@ -11,7 +11,8 @@ HEADER = os.path.join(ROOT, "include", "pagedecode.h")
 
 
 def _declared():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pd_[a-z_0-9]+)\s*\(", text)))
 
