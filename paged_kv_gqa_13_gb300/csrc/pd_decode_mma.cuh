@@ -110,17 +110,30 @@ __global__ void __launch_bounds__(256, 1)
 
     const uint64_t policy = l2_evict_first_policy();
     // Paged pools of pages of at most 16 rows, without the fused append: chunk
-    // s of this warp is position p0 + s, so the first stages' copies go out as
-    // soon as their page ids are known, before the table is staged (they take
-    // the place of the first-slab L2 prefetch). A bad page id is an
-    // out-of-range coordinate, which reads zeros; its chunk has no rows.
-    const int n_early = (!kFused && !kNhd && !a.contiguous && a.page_size <= kMmaRows)
-                            ? int(min((long long)kS, max(pend - p0, 0LL)))
-                            : 0;
+    // s of this warp is position p0 + s while those positions belong to
+    // requests, so the first stages' copies go out as soon as their page ids
+    // are known, before the table is staged (they take the place of the
+    // first-slab L2 prefetch). A bad page id is an out-of-range coordinate,
+    // which reads zeros; its chunk has no rows.
+    // Positions outside [indptr[0], indptr[batch]) (entries of `indices` that
+    // no request lists) have no chunk, so the early copies stop at the first
+    // such position: every position before it is one chunk, in order.
+    const bool early_ok = !kFused && !kNhd && !a.contiguous && a.page_size <= kMmaRows;
+    const int cov_lo = early_ok ? __ldg(a.indptr) : 0;
+    const int cov_hi = early_ok ? __ldg(a.indptr + a.batch) : 0;
+    int n_early = 0;
     walk.stage_table(s_indptr, s_lpl, [&] {
         if (lane == 0) {
             for (int s = 0; s < kS; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
+        }
+        if (early_ok) {
+            const long long lim = min((long long)kS, max(pend - p0, 0LL));
+            while (n_early < lim) {
+                const long long i = (p0 + n_early) % a.n_pos;
+                if (i < cov_lo || i >= cov_hi) break;
+                ++n_early;
+            }
         }
         if (n_early == 0) {
             walk.template prefetch_first_slabs<kNhd>(first_page, kS, size_t(D) * sizeof(T));

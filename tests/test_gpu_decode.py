@@ -278,3 +278,26 @@ def test_merge_states_all_parts_empty():
     lse = torch.zeros(5, device="cuda")
     pd.pd_merge_states(op, lp, o, lse)
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("lead,trail", [(0, 5), (2, 1)])  # both hit on 148- and 152-SM grids
+def test_indices_entries_that_no_request_lists(lead, trail):
+    """`indices` may hold entries outside [indptr[0], indptr[batch]) (the header
+    allows indptr[batch] < num_indices). Those positions have no chunk; with ~5
+    positions per warp, some warps start among them and run into the next
+    pass's listed pages, which the early first copies must not mistake for
+    their first chunks."""
+    import dataclasses
+
+    w = wl.make_paged("unlisted", "bf16", [2400, 2390, 2401, 2397], 32, 8, 128, 16, seed=96)
+    t = w.table
+    filler = t.indices[:max(lead, trail)]  # valid page ids that no request lists here
+    t2 = dataclasses.replace(t, indices=np.concatenate([filler[:lead], t.indices, filler[:trail]]).astype(np.int32),
+                             indptr=(t.indptr + lead).astype(np.int32))
+    dw = DeviceWorkload(w)
+    dw.set_table(t2)
+    o, lse = dw.decode()
+    assert dw.flags() == 0
+    o_ref, lse_ref = oracle.paged_decode(w.q, w.k_data, w.v_data, t2.indices, t2.indptr, t2.last_page_len,
+                                         w.num_qo_heads, w.num_kv_heads, w.head_dim, t2.page_size, w.sm_scale, "bf16")
+    compare(o, lse, o_ref, lse_ref, "bf16", f"{lead} leading, {trail} trailing unlisted entries")
