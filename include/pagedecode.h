@@ -40,7 +40,11 @@
  *    (page ids, indptr, last_page_len) are checked by the kernels: a bad
  *    value sets a bit of the sticky status word in the workspace header (see
  *    PD_FLAG_*), the offending page or request is treated as empty, and the
- *    kernel carries on. No kernel traps.
+ *    kernel carries on. No kernel traps. A malformed indptr (decreasing,
+ *    negative or past num_indices: PD_FLAG_BAD_INDPTR) makes request ranges
+ *    overlap or run off the table, so it leaves every output of that call
+ *    undefined, not only the flagged request's; the kernels still finish,
+ *    and later calls with a good table are unaffected.
  *  - Status codes: PD_ERR_INVALID for malformed extents or null pointers,
  *    PD_ERR_UNSUPPORTED for a head_dim, dtype or pointer alignment this
  *    library does not handle, PD_ERR_WORKSPACE for a missing or small
@@ -71,7 +75,7 @@ typedef enum {
 /* Bits of the sticky device status word (first int32 of every workspace). */
 #define PD_FLAG_BAD_PAGE_ID 0x1       /* a page id outside [0, num_total_pages): page treated as empty */
 #define PD_FLAG_BAD_LAST_PAGE_LEN 0x2 /* last_page_len outside [0, page_size]: clamped to that range */
-#define PD_FLAG_BAD_INDPTR 0x4        /* indptr decreasing, negative or past num_indices */
+#define PD_FLAG_BAD_INDPTR 0x4        /* indptr decreasing, negative or past num_indices: all outputs invalid */
 #define PD_FLAG_WAIT_TIMEOUT 0x8      /* a copy pipeline wait passed its time limit; outputs invalid */
 
 /* Bytes at the start of every workspace that hold the status word and the
@@ -87,6 +91,24 @@ typedef enum {
  */
 size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                                        pd_dtype dtype);
+
+/*
+ * Which decode kernel a call of this shape runs: one of PD_KERNEL_*. With
+ * fp8_pool nonzero the question is about pd_paged_decode_fp8 (dtype is then
+ * the type of q and o); otherwise about pd_paged_decode and the contiguous
+ * calls, which share their kernels. The group g = num_qo_heads / num_kv_heads
+ * is served in tiles of at most 8 q heads, padded to 1, 2, 4 or 8. 16-bit
+ * tiles of 4 or 8 run on tensor cores; f32 and 16-bit tiles of 1 or 2 run on
+ * CUDA cores. Over E4M3 pools, tiles of 4 or 8 at head_dim 128 or 256 run on
+ * the E4M3 tensor-core kernel, the rest on CUDA cores. This is a host-side
+ * lookup: it needs no device, enqueues nothing and returns PD_KERNEL_NONE for
+ * a shape that no call accepts.
+ */
+#define PD_KERNEL_NONE 0
+#define PD_KERNEL_CUDA_CORES 1
+#define PD_KERNEL_TENSOR_CORES 2
+#define PD_KERNEL_FP8_TENSOR_CORES 3
+int pd_decode_kernel_kind(int num_qo_heads, int num_kv_heads, int head_dim, pd_dtype dtype, int fp8_pool);
 
 /*
  * Batched paged decode (batch_paged_decode.rs: BatchPagedDecodePlan::run and
@@ -358,11 +380,13 @@ pd_status pd_profile_read(double* decode_ms, int* decode_launches, double* merge
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Each call clears the status word, then runs
- * the decode; the kernels' device-side table checks still run, but this
- * variant gives no way to read their flags. All calls share one array, so
- * calls whose kernels overlap on the GPU (different streams, or different
- * host threads) race on it: order them on one stream.
+ * before any stream capture. Each call that passes its argument checks
+ * clears the array's status word and then runs the decode; a call rejected
+ * by a check enqueues nothing. The kernels' device-side table checks set
+ * PD_FLAG_* bits in that word, which pd_paged_decode_noalloc_flags reads.
+ * All calls share one array, so calls whose kernels overlap on the GPU
+ * (different streams, or different host threads) race on it: order them on
+ * one stream.
  */
 pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, const void* v_data,
                                   const int32_t* indices, const int32_t* indptr,
@@ -370,6 +394,16 @@ pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, const void*
                                   int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                                   int num_total_pages, int num_indices, float sm_scale,
                                   pd_dtype dtype, void* stream);
+
+/*
+ * The status word of pd_paged_decode_noalloc's built-in scratch on the
+ * current device, read into *flags (host): the PD_FLAG_* bits that the last
+ * pd_paged_decode_noalloc call enqueued before this one set (a bad page id,
+ * last_page_len or indptr; a wait that ran out, after which the outputs are
+ * invalid). Synchronizes `stream`: enqueue it after that call, on the same
+ * stream. Allocates nothing. The word is cleared by the next noalloc call.
+ */
+pd_status pd_paged_decode_noalloc_flags(int32_t* flags, void* stream);
 
 /* Message for the last error status returned on this host thread ("" if none). */
 const char* pd_last_error_string(void);

@@ -30,6 +30,7 @@ PD_F32, PD_F16, PD_BF16 = 0, 1, 2
 PD_OK, PD_ERR_INVALID, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA = 0, 1, 2, 3, 4
 PD_FLAG_BAD_PAGE_ID, PD_FLAG_BAD_LAST_PAGE_LEN, PD_FLAG_BAD_INDPTR, PD_FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 PD_WORKSPACE_HEADER_BYTES = 256
+PD_KERNEL_NONE, PD_KERNEL_CUDA_CORES, PD_KERNEL_TENSOR_CORES, PD_KERNEL_FP8_TENSOR_CORES = 0, 1, 2, 3
 
 STATUS_NAMES = {0: "PD_OK", 1: "PD_ERR_INVALID", 2: "PD_ERR_UNSUPPORTED", 3: "PD_ERR_WORKSPACE",
                 4: "PD_ERR_CUDA"}
@@ -64,6 +65,8 @@ _SIGS = {
     "pd_contiguous_append_decode_nhd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
                                              _P]),
     "pd_paged_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "pd_paged_decode_noalloc_flags": (_I, [ctypes.POINTER(ctypes.c_int32), _P]),
+    "pd_decode_kernel_kind": (_I, [_I, _I, _I, _I, _I]),
     "pd_last_error_string": (ctypes.c_char_p, []),
     "pd_version": (_I, []),
 }
@@ -202,6 +205,19 @@ def pd_paged_decode_noalloc(q, k_data, v_data, indices, indptr, last_page_len, o
         _ptr(q), _ptr(k_data), _ptr(v_data), _ptr(indices) if indices.numel() else None, _ptr(indptr),
         _ptr(last_page_len), _ptr(o), _ptr(lse), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
         num_total_pages, indices.numel(), float(sm_scale), _dtype_code(q), _stream(stream)))
+
+
+def pd_paged_decode_noalloc_flags(stream=None) -> int:
+    """PD_FLAG_* bits set by the last pd_paged_decode_noalloc call on this device (synchronizes the stream)."""
+    v = ctypes.c_int32(0)
+    _check(_lib.pd_paged_decode_noalloc_flags(ctypes.byref(v), _stream(stream)))
+    return v.value
+
+
+def pd_decode_kernel_kind(num_qo_heads: int, num_kv_heads: int, head_dim: int, dtype: int,
+                          fp8_pool: bool = False) -> int:
+    """The PD_KERNEL_* a decode of this shape runs (host-side lookup; no device needed)."""
+    return _lib.pd_decode_kernel_kind(num_qo_heads, num_kv_heads, head_dim, dtype, 1 if fp8_pool else 0)
 
 
 def pd_paged_append(k_new, v_new, k_data, v_data, indices, indptr, last_page_len, workspace,

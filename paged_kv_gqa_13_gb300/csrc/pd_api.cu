@@ -584,6 +584,20 @@ size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_h
     return p.ws_bytes;
 }
 
+int pd_decode_kernel_kind(int num_qo_heads, int num_kv_heads, int head_dim, pd_dtype dtype, int fp8_pool) {
+    if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0) return PD_KERNEL_NONE;
+    if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return PD_KERNEL_NONE;
+    if (fp8_pool && dtype == PD_F32) return PD_KERNEL_NONE;
+    // the tile rule of make_plan_uncached; the lookups only take kernel addresses
+    int tiles = 0, per = 0;
+    split_group(num_qo_heads / num_kv_heads, &tiles, &per);
+    int G = 1;
+    while (G < per) G *= 2;
+    pd::KernelSet ks{};
+    if (!(fp8_pool ? lookup_fp8(dtype, head_dim, G, &ks) : lookup(dtype, head_dim, G, &ks))) return PD_KERNEL_NONE;
+    return ks.mma == 2 ? PD_KERNEL_FP8_TENSOR_CORES : ks.mma == 1 ? PD_KERNEL_TENSOR_CORES : PD_KERNEL_CUDA_CORES;
+}
+
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                                             pd_dtype dtype) {
     Plan p;
@@ -600,7 +614,7 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
                                    int num_kv_heads, int head_dim, int page_size, int num_total_pages,
                                    int num_indices, float sm_scale, pd_dtype dtype, void* workspace,
                                    size_t workspace_bytes, void* stream, const float* k_scale = nullptr,
-                                   const float* v_scale = nullptr) {
+                                   const float* v_scale = nullptr, bool clear_header = false) {
     const bool fp8 = k_scale != nullptr;
     if (dtype != PD_F32 && dtype != PD_F16 && dtype != PD_BF16) return fail(PD_ERR_UNSUPPORTED, "dtype must be PD_F32, PD_F16 or PD_BF16");
     if (batch <= 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_total_pages <= 0)
@@ -652,6 +666,13 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     a.slab_rows = page_size;
     a.k_new = k_new;
     a.v_new = v_new;
+    if (clear_header) {
+        // Every check has passed: zero the status word and the tail counters
+        // (a workspace whose header the caller cannot clear itself).
+        const cudaError_t e =
+            cudaMemsetAsync(workspace, 0, PD_WORKSPACE_HEADER_BYTES, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+    }
     return launch_decode(pl, a, head_dim, dtype, num_total_pages, false, static_cast<cudaStream_t>(stream));
 }
 
@@ -1071,10 +1092,22 @@ extern "C" pd_status pd_paged_decode_noalloc(const void* q, const void* k_data, 
                     "this shape needs %zu bytes of decode scratch; pd_paged_decode_noalloc has %zu "
                     "(use pd_paged_decode with a caller workspace)",
                     pl.ws_bytes, kNoAllocScratchBytes);
-    // The array keeps the last call's contents; the status word must start at zero.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, PD_WORKSPACE_HEADER_BYTES, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch header");
-    return pd_paged_decode(q, k_data, v_data, indices, indptr, last_page_len, o, lse, batch, num_qo_heads,
-                           num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale, dtype,
-                           scratch, kNoAllocScratchBytes, stream);
+    // The array keeps the last call's contents: its header (status word and
+    // tail counters) is cleared once every argument check has passed, just
+    // before the launch, so a rejected call enqueues nothing.
+    return paged_decode_impl(q, nullptr, nullptr, k_data, v_data, indices, indptr, last_page_len, o, lse, batch,
+                             num_qo_heads, num_kv_heads, head_dim, page_size, num_total_pages, num_indices, sm_scale,
+                             dtype, scratch, kNoAllocScratchBytes, stream, nullptr, nullptr, true);
+}
+
+extern "C" pd_status pd_paged_decode_noalloc_flags(int32_t* flags, void* stream) {
+    if (!flags) return fail(PD_ERR_INVALID, "null pointer argument");
+    void* scratch = nullptr;
+    pd_status st = noalloc_scratch(&scratch);
+    if (st != PD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flags, scratch, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the static scratch status word");
+    return ok();
 }

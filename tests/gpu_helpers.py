@@ -102,3 +102,45 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype: str, what: str = ""):
             dl = float(np.max(np.abs(lg[~empty] - lse_ref[~empty])))
         assert dl <= LSE_TOL, f"{what}: max |lse - lse_ref| = {dl:.3g} > {LSE_TOL}"
     return do, dl
+
+
+class Fp8Device:
+    """A workload's E4M3 pool (codes and per-kv-head scales) on the GPU, with outputs and workspace."""
+
+    def __init__(self, w):
+        import torch
+
+        import paged_kv_gqa_13_gb300 as pd
+        import workloads as wl
+
+        self.w = w
+        self.k8, self.v8, self.ks, self.vs = wl.fp8_pool(w)
+        self.q = to_dev(w.q, w.dtype)
+        self.k = torch.from_numpy(self.k8).cuda()
+        self.v = torch.from_numpy(self.v8).cuda()
+        self.ksd = torch.from_numpy(self.ks).cuda()
+        self.vsd = torch.from_numpy(self.vs).cuda()
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device="cuda")
+        self.ws = pd.alloc_workspace(pd.pd_paged_decode_fp8_workspace_bytes(
+            w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, {"f16": pd.PD_F16, "bf16": pd.PD_BF16}[w.dtype]))
+        self.set_table(w.table)
+
+    def set_table(self, t):
+        self.t = t
+        self.ind, self.ptr, self.lpl = table_dev(t)
+
+    def decode(self):
+        import paged_kv_gqa_13_gb300 as pd
+
+        pd.pd_paged_decode_fp8(self.q, self.k, self.v, self.ksd, self.vsd, self.ind, self.ptr, self.lpl, self.o,
+                               self.lse, self.w.sm_scale, self.ws)
+        return self.o, self.lse
+
+    def oracle_decode(self, k8=None, v8=None):
+        import oracle
+
+        t, w = self.t, self.w
+        return oracle.paged_decode_fp8(w.q, self.k8 if k8 is None else k8, self.v8 if v8 is None else v8, self.ks,
+                                       self.vs, t.indices, t.indptr, t.last_page_len, w.num_qo_heads,
+                                       w.num_kv_heads, w.head_dim, t.page_size, w.sm_scale, w.dtype)

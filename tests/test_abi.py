@@ -126,3 +126,44 @@ def test_a_c_program_compiles_links_and_runs_against_the_header(tmp_path):
     env = dict(os.environ)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, env=env).stdout.split()
     assert out == [str(len(names)), "1", "str"]
+
+
+def _expected_kind(hq, hk, d, dtype, fp8):
+    """The dispatch rule, written out: the group is cut into the fewest equal
+    tiles of at most 8 heads, padded to 1, 2, 4 or 8; 16-bit tiles of 4 or 8
+    run on tensor cores; over E4M3 pools only at head_dim 128 or 256."""
+    import paged_kv_gqa_13_gb300 as pd
+
+    if hq <= 0 or hk <= 0 or hq % hk or d not in (64, 128, 256) or (fp8 and dtype == pd.PD_F32):
+        return pd.PD_KERNEL_NONE
+    g = hq // hk
+    tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
+    pad = 1 << (g // tiles - 1).bit_length()
+    if fp8:
+        return pd.PD_KERNEL_FP8_TENSOR_CORES if (d >= 128 and pad >= 4) else pd.PD_KERNEL_CUDA_CORES
+    return pd.PD_KERNEL_TENSOR_CORES if (dtype != pd.PD_F32 and pad >= 4) else pd.PD_KERNEL_CUDA_CORES
+
+
+def test_decode_kernel_kind_follows_the_dispatch_rule():
+    """pd_decode_kernel_kind is a host-side lookup (no device needed); the GPU
+    tests use it to check which kernel their shapes reach."""
+    import paged_kv_gqa_13_gb300 as pd
+
+    k = pd.pd_decode_kernel_kind
+    # the shapes of the workloads
+    assert k(32, 8, 128, pd.PD_BF16) == pd.PD_KERNEL_TENSOR_CORES        # Llama-3-8B, group 4
+    assert k(64, 8, 128, pd.PD_BF16) == pd.PD_KERNEL_TENSOR_CORES        # 70B, group 8
+    assert k(16, 16, 256, pd.PD_F16) == pd.PD_KERNEL_CUDA_CORES          # MHA D 256
+    assert k(8, 2, 64, pd.PD_F32) == pd.PD_KERNEL_CUDA_CORES             # tiny f32
+    assert k(32, 8, 128, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES
+    assert k(32, 8, 64, pd.PD_BF16, True) == pd.PD_KERNEL_CUDA_CORES     # E4M3 at D 64
+    assert k(8, 3, 128, pd.PD_F16) == pd.PD_KERNEL_NONE                  # not a multiple
+    assert k(8, 2, 96, pd.PD_F16) == pd.PD_KERNEL_NONE                   # head_dim
+    assert k(8, 2, 128, pd.PD_F32, True) == pd.PD_KERNEL_NONE            # E4M3 takes 16-bit q
+    for dtype in (pd.PD_F32, pd.PD_F16, pd.PD_BF16):
+        for d in (64, 96, 128, 256):
+            for hk in (1, 2, 8):
+                for g in range(1, 25):
+                    for fp8 in (False, True):
+                        assert k(g * hk, hk, d, dtype, fp8) == _expected_kind(g * hk, hk, d, dtype, fp8), \
+                            (g, hk, d, dtype, fp8)

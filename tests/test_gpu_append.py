@@ -136,7 +136,7 @@ def test_contiguous_append_rejects_position_past_the_cache():
 
 @pytest.mark.parametrize("dtype,Hq,Hk,D", [
     ("f16", 16, 16, 256),   # MHA, CUDA cores
-    ("bf16", 32, 8, 128),   # group 4, CUDA cores
+    ("bf16", 32, 8, 128),   # group 4, tensor cores
     ("bf16", 64, 8, 128),   # group 8, tensor cores
     ("bf16", 32, 2, 128),   # group 16: two head tiles write the same row, tensor cores
     ("f32", 24, 2, 64),     # group 12: two head tiles of 6, CUDA cores

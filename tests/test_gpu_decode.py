@@ -62,7 +62,12 @@ def test_dtype_headdim_group_grid(dtype, head_dim, hq, hk):
 @pytest.mark.parametrize("page_size", [1, 8, 16, 32, 64, 100])
 @pytest.mark.parametrize("hq,hk,dtype", [(16, 4, "bf16"), (16, 2, "bf16"), (16, 2, "f16")])
 def test_page_sizes(page_size, hq, hk, dtype):
-    # group 4 runs on CUDA cores, group 8 on the tensor-core kernel (16-row TMA boxes)
+    # Groups 4 and 8 in 16 bits both run on the tensor-core kernel (16-row TMA
+    # boxes); the CUDA-core kernel's page sizes are in test_gpu_cuda_core_pages.py.
+    import paged_kv_gqa_13_gb300 as pd
+
+    assert pd.pd_decode_kernel_kind(hq, hk, 128, {"f16": pd.PD_F16, "bf16": pd.PD_BF16}[dtype]) == \
+        pd.PD_KERNEL_TENSOR_CORES
     w = wl.make_paged(f"pages_{page_size}", dtype, [1, page_size, 2 * page_size, 333, 50, 17], hq, hk, 128,
                       page_size, seed=40 + page_size)
     _run(w)
@@ -138,6 +143,39 @@ def test_bad_page_id_and_last_page_len_are_flagged_not_fatal():
     dw.set_table(t3)
     dw.decode()
     assert dw.flags() & pd.PD_FLAG_BAD_INDPTR
+
+
+@pytest.mark.parametrize("how", ["a range ends before it starts", "indptr[batch] below indptr[0]"])
+def test_decreasing_indptr_is_flagged_and_the_next_call_is_clean(how):
+    """A decreasing indptr on the tensor-core kernel (group 4, pages of 16
+    rows), whose first copies go out before the table is staged, with shares
+    long enough to take tails. The call finishes and sets PD_FLAG_BAD_INDPTR
+    (its outputs are then undefined); the next call with the good table, on the
+    same workspace after pd_workspace_init, gives bit for bit what it gave
+    before the bad call, with no flag: the context, the workspace and its tail
+    counters are intact."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.llama3_8b_bf16(seed=57, batch=24, lo=1000, hi=4000)
+    dw = DeviceWorkload(w)
+    o_good, l_good = (x.clone() for x in dw.decode())
+    compare(o_good, l_good, *oracle.paged_decode_workload(w), "bf16", "good table")
+    bad = w.table.copy()
+    if how == "a range ends before it starts":
+        bad.indptr[5] = bad.indptr[4] - 50
+    else:
+        bad.indptr[0] = 40
+        bad.indptr[-1] = 20
+    dw.set_table(bad)
+    dw.decode()
+    assert dw.flags() & pd.PD_FLAG_BAD_INDPTR
+    pd.pd_workspace_init(dw.ws)
+    dw.set_table(w.table)
+    o2, l2 = dw.decode()
+    assert dw.flags() == 0
+    assert torch.equal(o2.view(torch.int16), o_good.view(torch.int16)) and torch.equal(l2, l_good)
 
 
 def test_repeated_calls_are_bit_identical():
