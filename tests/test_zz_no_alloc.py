@@ -63,3 +63,33 @@ def test_noalloc_rejects_a_shape_above_its_scratch():
     with pytest.raises(pd.PagedecodeError) as ei:
         pd.pd_paged_decode_noalloc(q, k, k, ind, ptr, lpl, q, lse, 0.1)
     assert ei.value.status == pd.PD_ERR_WORKSPACE and "16777216" in str(ei.value)
+
+
+def test_noalloc_flags_are_readable_and_a_rejected_call_enqueues_nothing():
+    """The device-side table checks of a noalloc call are read back with
+    pd_paged_decode_noalloc_flags. A call that fails its host-side argument
+    checks enqueues nothing, not even the clearing of the status word, so the
+    previous call's flags are still there after it."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("noalloc_flags", "bf16", [40, 40, 300], 8, 2, 128, 16, seed=94)
+    dw = DeviceWorkload(w)
+    o_ref, lse_ref = (x.clone() for x in dw.decode())
+    o, lse = torch.empty_like(dw.o), torch.empty_like(dw.lse)
+    pd.pd_paged_decode_noalloc(dw.q, dw.k, dw.v, dw.indices, dw.indptr, dw.lpl, o, lse, w.sm_scale)
+    assert pd.pd_paged_decode_noalloc_flags() == 0
+    bad = w.table.copy()
+    bad.indices[1] = w.table.num_total_pages + 3  # a page id outside the pool
+    dw.set_table(bad)
+    pd.pd_paged_decode_noalloc(dw.q, dw.k, dw.v, dw.indices, dw.indptr, dw.lpl, o, lse, w.sm_scale)
+    assert pd.pd_paged_decode_noalloc_flags() == pd.PD_FLAG_BAD_PAGE_ID
+    with pytest.raises(pd.PagedecodeError) as ei:  # lse missing: rejected on the host
+        pd.pd_paged_decode_noalloc(dw.q, dw.k, dw.v, dw.indices, dw.indptr, dw.lpl, o, None, w.sm_scale)
+    assert ei.value.status == pd.PD_ERR_INVALID
+    assert pd.pd_paged_decode_noalloc_flags() == pd.PD_FLAG_BAD_PAGE_ID
+    dw.set_table(w.table)
+    pd.pd_paged_decode_noalloc(dw.q, dw.k, dw.v, dw.indices, dw.indptr, dw.lpl, o, lse, w.sm_scale)
+    assert pd.pd_paged_decode_noalloc_flags() == 0
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(lse, lse_ref)
