@@ -1,8 +1,8 @@
 // Batched decode attention over a paged (or contiguous) KV cache on CUDA
-// cores: the kernel for f32, for 16-bit groups of up to 4 q heads per kv head
-// when each warp's share is short (tiles of 4 with long shares run on tensor
-// cores), and, as a variant, for E4M3 pools outside the tensor-core kernel's
-// shapes.
+// cores: the kernel for f32 at every group, for 16-bit tiles of 1 or 2 q
+// heads per kv head (16-bit tiles of 4 to 8 heads run on the tensor-core
+// kernel, pd_decode_mma.cuh), and, as a variant, for E4M3 pools outside the
+// E4M3 tensor-core kernel's shapes.
 //
 // Work decomposition (see pd_walk.cuh). All positions of the call are cut into
 // equal contiguous ranges, one per warp of a grid that fills every SM. A warp

@@ -1,7 +1,8 @@
-// Batched decode attention on tensor cores, for tiles of up to 8 q heads per
-// kv head in f16 / bf16: group sizes 5..8 (and larger groups cut into tiles of
-// 8) always, and tiles of 4 when each warp streams long work (the host's
-// choice per call). At group 8 the per-byte arithmetic (2 x 8 FMAs per K/V element pair)
+// Batched decode attention on tensor cores, for 16-bit (f16 / bf16) tiles of
+// 4 to 8 q heads per kv head: groups 3..8 (a tile of 3 or 4 heads is padded to
+// the 8-head tile) and larger groups cut into tiles of at most 8. Tiles of 1
+// or 2 heads and f32 run on CUDA cores (pd_decode.cuh). At group 8 the
+// per-byte arithmetic (2 x 8 FMAs per K/V element pair)
 // saturates the CUDA cores, while the grouped score tile S = K q^T
 // (16 tokens x 8 heads x head_dim) and O^T += V^T P (head_dim x 8 heads x 16
 // tokens) are small dense contractions that the mma.sync m16n8k16 units do in
