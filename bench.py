@@ -14,6 +14,11 @@ host buffers, and SM clocks sampled during the run.
 runnable reference implementation) on a bounded sample of the same workload.
 Under torchrun every rank runs its own replica on its own GPU (the decode has
 no exchange step); rank 0 prints.
+
+On one GPU the line also carries `per_config`: the long-context batch (paged
+and contiguous entries), the ragged 70B-shaped batch and the MHA append +
+decode step, each timed the same way in the same process after the headline
+workload (--no-per-config skips them).
 """
 from __future__ import annotations
 
@@ -73,36 +78,46 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle samples while the benchmark runs."""
+    """nvidia-smi SM clock / throttle samples while the benchmark runs.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    nvidia-smi runs as its own process and writes its samples (each with its
+    own timestamp) to a file, which is read after the run: no thread of this
+    process competes with the launch loop while it is timed."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.samples = []
+        import tempfile
+
         self.marks = {}
+        fd, self.path = tempfile.mkstemp(prefix="pd_clocks_", suffix=".csv")
+        os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
-                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-i", str(gpu_index), "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
-
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append((time.time(), parts))
 
     def mark(self, name):
         self.marks[name] = time.time()
 
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def stop(self) -> dict:
         if self.proc is None:
+            os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.proc.terminate()
@@ -110,11 +125,18 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        samples = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    samples.append((self._when(parts[0]), parts[1:]))
+        os.unlink(self.path)
         t0, t1 = self.marks.get("timed_start", 0), self.marks.get("timed_end", 1e30)
-        timed = [p for (t, p) in self.samples if t0 <= t <= t1]
+        timed = [p for (t, p) in samples if t is not None and t0 <= t <= t1]
         window = "timed region"
         if not timed:
-            timed = [p for (_, p) in self.samples]
+            timed = [p for (_, p) in samples]
             window = "whole run (timed region shorter than the 100 ms sampling period)"
 
         def num(x):
@@ -169,33 +191,47 @@ def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
+# Extra workloads timed in the same process after the headline one (one GPU
+# only): the long-context batch through the paged and the contiguous entry,
+# the ragged 70B-shaped batch and the MHA append + decode step.
+PER_CONFIG = ["long_context", "long_context_contiguous", "ragged_70b", "mha_append"]
+# Host lead before the timed steps: the stream first runs a spin kernel of
+# this length, so that every timed step is already queued when the GPU
+# reaches it and no host pause (GC, a thread switch) lands inside a step.
+PREROLL_S = 5e-3
+
+
+def to_dev(raw, dtype, device):
+    import torch
+
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(raw)).to(device)
+    t = torch.from_numpy(np.ascontiguousarray(raw).view(np.int16)).to(device)
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
+
+
+def table_dev(t, device):
+    import torch
+
+    return tuple(torch.from_numpy(x.astype(np.int32)).to(device) for x in (t.indices, t.indptr, t.last_page_len))
+
+
+def setup_config(args, name: str, rank: int, dev) -> dict:
+    """Device copies of one workload and its step function: the library call a
+    step makes, and the algorithmic bytes per step (all kernels, and the decode
+    kernel's own)."""
     import torch
 
     import paged_kv_gqa_13_gb300 as pd
     import workloads as wl
 
-    def to_dev(raw, dtype, device):
-        if dtype == "f32":
-            return torch.from_numpy(np.ascontiguousarray(raw)).to(device)
-        t = torch.from_numpy(np.ascontiguousarray(raw).view(np.int16)).to(device)
-        return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
-
-    def table_dev(t, device):
-        return tuple(torch.from_numpy(x.astype(np.int32)).to(device)
-                     for x in (t.indices, t.indptr, t.last_page_len))
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w, mode = load_workload(args.config, rank)
+    w, mode = load_workload(name, rank)
     code = {"f32": pd.PD_F32, "f16": pd.PD_F16, "bf16": pd.PD_BF16}[w.dtype]
-    stream = torch.cuda.current_stream()
-
+    c = {"w": w, "mode": mode, "tables": [w.table]}
     q = to_dev(w.q, w.dtype, dev)
     o = torch.empty_like(q)
     lse = torch.empty(w.batch, w.num_qo_heads, dtype=torch.float32, device=dev)
-    tables = [w.table]
-    appends = []
+    c.update(q=q, o=o, lse=lse)
     if mode.startswith("contiguous"):
         kc, vc, n_valid = wl.contiguous_copy(w)
         k = to_dev(kc, w.dtype, dev)
@@ -210,8 +246,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
 
         def step(i):
             decode(q, k, v, o, lse, n_valid, w.sm_scale, ws)
-        bytes_per_step = [algorithmic_bytes(w)]
-        decode_bytes_per_step = bytes_per_step
+        c["bytes"] = [algorithmic_bytes(w)]
+        c["decode_bytes"] = c["bytes"]
     elif mode == "paged_fp8":
         k8, v8, ks, vs = wl.fp8_pool(w)
         k, v = torch.from_numpy(k8).to(dev), torch.from_numpy(v8).to(dev)
@@ -223,23 +259,25 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
 
         def step(i):
             pd.pd_paged_decode_fp8(q, k, v, ksd, vsd, ind, ptr, lpl, o, lse, w.sm_scale, ws)
-        bytes_per_step = [algorithmic_bytes(w, mode=mode)]
-        decode_bytes_per_step = bytes_per_step
+        c["bytes"] = [algorithmic_bytes(w, mode=mode)]
+        c["decode_bytes"] = c["bytes"]
     else:
         k = to_dev(w.k_data, w.dtype, dev)
         v = to_dev(w.v_data, w.dtype, dev)
         ws = pd.alloc_workspace(pd.pd_paged_decode_workspace_bytes(
             w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, code), dev)
+        tables, appends = [w.table], []
         if w.append_steps:
             # append-then-decode: each step appends one row per request, then decodes
             t = w.table
-            for s in range(w.append_steps):
+            for s_ in range(w.append_steps):
                 t = wl.table_after_append(t)
                 tables.append(t)
-                kn, vn = w.new_rows(s)
+                kn, vn = w.new_rows(s_)
                 appends.append((to_dev(kn, w.dtype, dev), to_dev(vn, w.dtype, dev)))
             tables = tables[1:]
         dev_tables = [table_dev(t, dev) for t in tables]
+        fused = args.append == "fused"
 
         # Step i uses table i mod steps. Repeating the sequence rewrites the same
         # rows with the same bytes, and a decode never reads rows appended later,
@@ -249,31 +287,189 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                 j = i % w.append_steps
                 ind, ptr, lpl = dev_tables[j]
                 kn, vn = appends[j]
-                if args.append == "fused":
+                if fused:
                     pd.pd_paged_append_decode(q, kn, vn, k, v, ind, ptr, lpl, o, lse, w.sm_scale, ws)
                     return
                 pd.pd_paged_append(kn, vn, k, v, ind, ptr, lpl, ws)
             else:
                 ind, ptr, lpl = dev_tables[0]
             pd.pd_paged_decode(q, k, v, ind, ptr, lpl, o, lse, w.sm_scale, ws)
-        bytes_per_step = [algorithmic_bytes(w, t) for t in tables]
-        decode_bytes_per_step = list(bytes_per_step)
+        c["tables"] = tables
+        c["bytes"] = [algorithmic_bytes(w, t) for t in tables]
+        c["decode_bytes"] = list(c["bytes"])
         if w.append_steps:
             ab = 2 * w.batch * w.num_kv_heads * w.head_dim * wl.ELEM_BYTES[w.dtype] * 2
-            bytes_per_step = [b + ab for b in bytes_per_step]
-            if args.append == "fused":  # the one kernel also moves the appended rows
-                decode_bytes_per_step = bytes_per_step
+            c["bytes"] = [b + ab for b in c["bytes"]]
+            if fused:  # the one kernel also moves the appended rows
+                c["decode_bytes"] = c["bytes"]
+    c.update(k=k, v=v, ws=ws, step=step)
+    return c
+
+
+def time_steps(c, steps: int, warmup: int, flush_l2, stream, barrier=None, sampler=None) -> dict:
+    """W warm-up steps, then K timed steps (one CUDA event pair each, L2
+    flushed before each outside the pair), then the same K steps again with
+    the library's own events around each kernel (an event between the decode
+    and merge launches would serialise the pair, so they are kept out of the
+    first pass)."""
+    import gc
+
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    step = c["step"]
+    for i in range(warmup):
+        flush_l2()
+        step(i)
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    preroll = int(PREROLL_S * 2.07e9)
+    gc.disable()
+    try:
+        if sampler is not None:
+            sampler.mark("timed_start")
+        torch.cuda._sleep(preroll)
+        for i in range(steps):
+            flush_l2()  # evict K/V of the previous step from L2 (outside the timed events)
+            starts[i].record(stream)
+            step(warmup + i)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.mark("timed_end")
+        if barrier is not None:
+            barrier()
+        pd.pd_profile_read()  # discard anything recorded before
+        pd.pd_profile_enable(True)
+        torch.cuda._sleep(preroll)
+        for i in range(steps):
+            flush_l2()
+            step(warmup + i)
+        torch.cuda.synchronize()
+    finally:
+        gc.enable()
+        pd.pd_profile_enable(False)
+    prof = pd.pd_profile_read()
+    ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+
+    def mean_of(xs):
+        return float(np.mean([xs[(warmup + i) % len(xs)] for i in range(steps)]))
+    return {"ms": ms, "ms_mean": float(np.mean(ms)), "prof": prof, "bytes_mean": mean_of(c["bytes"]),
+            "decode_bytes_mean": mean_of(c["decode_bytes"])}
+
+
+def kernel_roofline(c, t, peak_gbs: float) -> dict:
+    prof = t["prof"]
+    dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
+    achieved = t["decode_bytes_mean"] / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
+    return {"kernel": decode_kernel_name(c["w"], c["mode"]), "achieved": achieved,
+            "frac": achieved / peak_gbs if achieved else None, "kernel_us": dec_ms * 1e3,
+            "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
+            "append_us": (prof["append_ms"] / prof["append_launches"] * 1e3) if prof["append_launches"] else None}
+
+
+def step_stats(ms) -> dict:
+    us = np.asarray(ms) * 1e3
+    return {"us_p10_p50_p90": [float(np.percentile(us, x)) for x in (10, 50, 90)],
+            "us_p99_max": [float(np.percentile(us, 99)), float(us.max())]}
+
+
+def run_e2e(c, args, dev, flush_l2, stream):
+    """End to end through the C ABI with host buffers: per step, copy q and
+    the page table in from pinned host memory, decode with o and lse in pinned
+    host memory (the kernels' stores cross to the host; no copy back)."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w, q, o, lse, k, v, ws = c["w"], c["q"], c["o"], c["lse"], c["k"], c["v"], c["ws"]
+    # One step end to end: the step's inputs (q and the page table) go in
+    # from pinned host memory in one copy, and the decode writes o and lse
+    # straight into pinned host memory (reachable from kernels at the same
+    # address under unified addressing), which saves a ~7 us copy back. The
+    # KV cache is resident state, like weights.
+    t = c["tables"][0]
+    esz = q.element_size()
+    parts_in = [("q", q.numel() * esz), ("indices", 4 * t.num_indices), ("indptr", 4 * (w.batch + 1)),
+                ("lpl", 4 * w.batch)]
+    offs, n = {}, 0
+    for name, nb in parts_in:
+        offs[name] = n
+        n += (nb + 15) // 16 * 16  # keep every view 16-byte aligned
+    h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(n, dtype=torch.uint8, device=dev)
+    q_host = np.ascontiguousarray(w.q).view(np.uint8).reshape(-1)
+    h_in[offs["q"]:offs["q"] + q_host.size] = torch.from_numpy(q_host)
+    for name, arr in (("indices", t.indices), ("indptr", t.indptr), ("lpl", t.last_page_len)):
+        b = np.ascontiguousarray(arr.astype(np.int32)).view(np.uint8).reshape(-1)
+        h_in[offs[name]:offs[name] + b.size] = torch.from_numpy(b)
+
+    def view(buf, name, nbytes, dtype, shape):
+        return buf[offs[name]:offs[name] + nbytes].view(dtype).view(shape)
+    qd = view(d_in, "q", q.numel() * esz, q.dtype, q.shape)
+    ind_d = view(d_in, "indices", 4 * t.num_indices, torch.int32, (t.num_indices,))
+    ptr_d = view(d_in, "indptr", 4 * (w.batch + 1), torch.int32, (w.batch + 1,))
+    lpl_d = view(d_in, "lpl", 4 * w.batch, torch.int32, (w.batch,))
+    ob = o.numel() * esz
+    h_out = torch.empty(ob + 4 * lse.numel(), dtype=torch.uint8).pin_memory()
+    oh = h_out[:ob].view(q.dtype).view(o.shape)
+    lseh = h_out[ob:].view(torch.float32).view(lse.shape)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    host_s = []
+    for i in range(args.warmup + args.steps):
+        if i >= args.warmup:
+            flush_l2()
+            es[2 * (i - args.warmup)].record(stream)
+        h0 = time.perf_counter()
+        d_in.copy_(h_in, non_blocking=True)
+        pd.pd_paged_decode(qd, k, v, ind_d, ptr_d, lpl_d, oh, lseh, w.sm_scale, ws)
+        host_s.append(time.perf_counter() - h0)
+        if i >= args.warmup:
+            es[2 * (i - args.warmup) + 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([es[2 * j].elapsed_time(es[2 * j + 1]) for j in range(args.steps)]))
+    # the host-resident result must be the one a device-resident decode gives
+    o_dev, lse_dev = torch.empty_like(oh, device=dev), torch.empty_like(lseh, device=dev)
+    pd.pd_paged_decode(qd, k, v, ind_d, ptr_d, lpl_d, o_dev, lse_dev, w.sm_scale, ws)
+    torch.cuda.synchronize()
+    if not (torch.equal(oh.view(torch.uint8), o_dev.cpu().view(torch.uint8)) and torch.equal(lseh, lse_dev.cpu())):
+        raise RuntimeError("e2e: the decode into pinned host memory differs from the device-resident decode")
+    bytes_mean = float(np.mean(c["bytes"]))
+    return {"value": bytes_mean / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+            "h2d_bytes_per_step": int(n), "d2h_bytes_per_step": int(h_out.numel()),
+            "d2h": "o and lse stored by the kernels into pinned host memory",
+            "host_us_per_step": 1e6 * float(np.median(host_s[args.warmup:]))}
+
+
+def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    c = setup_config(args, args.config, rank, dev)
 
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2():
         # Write a buffer 4x the L2 (evicts every line of the last step), then
         # read one 2x the L2 so that the dirty lines of that write are written
         # back here, not inside the next timed step: the step starts with a
-        # cold, clean L2.
+        # cold, clean L2. The sum goes into a tensor allocated up front: a
+        # first allocation inside the timed loop would call cudaMalloc, which
+        # waits for the device and leaves the step after it without a host
+        # lead (one 160 us step in 20, measured).
         flush_w.zero_()
-        flush_r.sum()
+        torch.sum(flush_r, dim=0, out=flush_out)
 
     # in-process copy-kernel bandwidth (reported beside the measured peak of MEASURED_PEAKS.json)
     copy_gbs = None
@@ -294,108 +490,36 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     entries = [x.strip() for x in visible.split(",") if x.strip()]
     sampler = ClockSampler(entries[local_rank] if local_rank < len(entries) else local_rank)
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler.mark("timed_start")
+    barrier = torch.distributed.barrier if world > 1 else None
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2()  # evict K/V of the previous step from L2 (outside the timed events)
-        starts[i].record(stream)
-        step(args.warmup + i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    t = time_steps(c, args.steps, args.warmup, flush_l2, stream, barrier, sampler)
     t_wall = time.perf_counter() - t_wall
-    sampler.mark("timed_end")
-    if world > 1:
-        torch.distributed.barrier()
-    # Kernel durations: the same K steps again with the library recording CUDA
-    # events around each of its kernels. Kept out of the pass above because an
-    # event between the decode and the merge launch serialises the pair.
-    pd.pd_profile_read()  # discard anything recorded before
-    pd.pd_profile_enable(True)
-    for i in range(args.steps):
-        flush_l2()
-        step(args.warmup + i)
-    torch.cuda.synchronize()
-    pd.pd_profile_enable(False)
-    prof = pd.pd_profile_read()
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_mean = float(np.mean(ms))
-    byte_steps = [bytes_per_step[(args.warmup + i) % len(bytes_per_step)] for i in range(args.steps)]
-    bytes_mean = float(np.mean(byte_steps))
-    decode_bytes_mean = float(np.mean([decode_bytes_per_step[(args.warmup + i) % len(decode_bytes_per_step)]
-                                       for i in range(args.steps)]))
-
-    # end to end through the C ABI with host buffers: per step, copy q and the
-    # page table in from pinned host memory, decode with o and lse in pinned
-    # host memory (the kernels' stores cross to the host; no copy back).
     e2e = None
-    if mode == "paged" and not w.append_steps and not args.quick:
-        # One step end to end: the step's inputs (q and the page table) go in
-        # from pinned host memory in one copy, and the decode writes o and lse
-        # straight into pinned host memory (reachable from kernels at the same
-        # address under unified addressing), which saves a ~7 us copy back. The
-        # KV cache is resident state, like weights.
-        t = tables[0]
-        esz = q.element_size()
-        parts_in = [("q", q.numel() * esz), ("indices", 4 * t.num_indices), ("indptr", 4 * (w.batch + 1)),
-                    ("lpl", 4 * w.batch)]
-        offs, n = {}, 0
-        for name, nb in parts_in:
-            offs[name] = n
-            n += (nb + 15) // 16 * 16  # keep every view 16-byte aligned
-        h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
-        d_in = torch.empty(n, dtype=torch.uint8, device=dev)
-        q_host = np.ascontiguousarray(w.q).view(np.uint8).reshape(-1)
-        h_in[offs["q"]:offs["q"] + q_host.size] = torch.from_numpy(q_host)
-        for name, arr in (("indices", t.indices), ("indptr", t.indptr), ("lpl", t.last_page_len)):
-            b = np.ascontiguousarray(arr.astype(np.int32)).view(np.uint8).reshape(-1)
-            h_in[offs[name]:offs[name] + b.size] = torch.from_numpy(b)
-
-        def view(buf, name, nbytes, dtype, shape):
-            return buf[offs[name]:offs[name] + nbytes].view(dtype).view(shape)
-        qd = view(d_in, "q", q.numel() * esz, q.dtype, q.shape)
-        ind_d = view(d_in, "indices", 4 * t.num_indices, torch.int32, (t.num_indices,))
-        ptr_d = view(d_in, "indptr", 4 * (w.batch + 1), torch.int32, (w.batch + 1,))
-        lpl_d = view(d_in, "lpl", 4 * w.batch, torch.int32, (w.batch,))
-        ob = o.numel() * esz
-        h_out = torch.empty(ob + 4 * lse.numel(), dtype=torch.uint8).pin_memory()
-        oh = h_out[:ob].view(q.dtype).view(o.shape)
-        lseh = h_out[ob:].view(torch.float32).view(lse.shape)
-        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-        host_s = []
-        for i in range(args.warmup + args.steps):
-            if i >= args.warmup:
-                flush_l2()
-                es[2 * (i - args.warmup)].record(stream)
-            h0 = time.perf_counter()
-            d_in.copy_(h_in, non_blocking=True)
-            pd.pd_paged_decode(qd, k, v, ind_d, ptr_d, lpl_d, oh, lseh, w.sm_scale, ws)
-            host_s.append(time.perf_counter() - h0)
-            if i >= args.warmup:
-                es[2 * (i - args.warmup) + 1].record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = float(np.mean([es[2 * j].elapsed_time(es[2 * j + 1]) for j in range(args.steps)]))
-        # the host-resident result must be the one a device-resident decode gives
-        o_dev, lse_dev = torch.empty_like(oh, device=dev), torch.empty_like(lseh, device=dev)
-        pd.pd_paged_decode(qd, k, v, ind_d, ptr_d, lpl_d, o_dev, lse_dev, w.sm_scale, ws)
-        torch.cuda.synchronize()
-        if not (torch.equal(oh.view(torch.uint8), o_dev.cpu().view(torch.uint8)) and torch.equal(lseh, lse_dev.cpu())):
-            raise RuntimeError("e2e: the decode into pinned host memory differs from the device-resident decode")
-        e2e = {"value": bytes_mean / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(n), "d2h_bytes_per_step": int(h_out.numel()),
-               "d2h": "o and lse stored by the kernels into pinned host memory",
-               "host_us_per_step": 1e6 * float(np.median(host_s[args.warmup:]))}
+    if c["mode"] == "paged" and not c["w"].append_steps and not args.quick:
+        e2e = run_e2e(c, args, dev, flush_l2, stream)
     clocks = sampler.stop()
-    return {"w": w, "mode": mode, "ms_mean": ms_mean, "ms_all": ms, "bytes_mean": bytes_mean,
-            "decode_bytes_mean": decode_bytes_mean, "prof": prof,
-            "copy_gbs": copy_gbs, "e2e": e2e, "clocks": clocks, "t_wall": t_wall}
+    out = {"w": c["w"], "mode": c["mode"], "ms_mean": t["ms_mean"], "ms_all": t["ms"], "bytes_mean": t["bytes_mean"],
+           "decode_bytes_mean": t["decode_bytes_mean"], "prof": t["prof"], "copy_gbs": copy_gbs, "e2e": e2e,
+           "clocks": clocks, "t_wall": t_wall, "per_config": None}
+    if world == 1 and args.per_config and not args.quick:
+        del c
+        torch.cuda.empty_cache()
+        peak = measured_peaks()["hbm_gbs"]
+        per = {}
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            pc = setup_config(args, name, rank, dev)
+            tp = time_steps(pc, args.steps, args.warmup, flush_l2, stream)
+            kr = kernel_roofline(pc, tp, peak)
+            tbps = tp["bytes_mean"] / (tp["ms_mean"] * 1e-3) / 1e12
+            per[name] = {"workload": pc["w"].name, "mode": pc["mode"], "us_per_call": tp["ms_mean"] * 1e3,
+                         **step_stats(tp["ms"]), "tbps": tbps, "pct_of_peak": 100.0 * tbps * 1e3 / peak,
+                         "bytes_per_step": int(tp["bytes_mean"]), **kr}
+            del pc
+            torch.cuda.empty_cache()
+        out["per_config"] = per
+    return out
 
 
 def slowest_rank_ms(ms_local: float, world: int) -> float:
@@ -464,6 +588,8 @@ def main():
     ap.add_argument("--append", default="fused", choices=["fused", "separate"],
                     help="append workloads: one fused append + decode launch, or an append launch then a decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the extra workloads timed after the headline one (one GPU only)")
     ap.add_argument("--quick", action="store_true",
                     help="decode steps only: no copy-peak, end-to-end or CPU-baseline legs (for profiler runs)")
     args = ap.parse_args()
@@ -504,17 +630,13 @@ def main():
     tbps = whole_job_tbps(r["bytes_mean"], ms_max, world)
     peaks = measured_peaks()
     prof = r["prof"]
-    dec_ms = prof["decode_ms"] / max(1, prof["decode_launches"])
-    dec_bytes = r["decode_bytes_mean"]  # the decode kernel's own bytes (no append rows)
-    achieved_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9 if dec_ms > 0 else None
-    kname = decode_kernel_name(w, r["mode"])
-    traffic = recorded_traffic(kname, w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd",
-                                                 "paged_fp8": "/e4m3"}.get(r["mode"], "")))
-    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved_gbs / peaks["hbm_gbs"] if achieved_gbs else None, "traffic": traffic,
-                "peak_source": peaks["source"], "kernel": kname,
-                "kernel_us": dec_ms * 1e3, "merge_us": prof["merge_ms"] / max(1, prof["merge_launches"]) * 1e3,
-                "append_us": (prof["append_ms"] / prof["append_launches"] * 1e3) if prof["append_launches"] else None,
+    kr = kernel_roofline({"w": w, "mode": r["mode"]}, {"prof": prof, "decode_bytes_mean": r["decode_bytes_mean"]},
+                         peaks["hbm_gbs"])
+    traffic = recorded_traffic(kr["kernel"], w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd",
+                                                        "paged_fp8": "/e4m3"}.get(r["mode"], "")))
+    roofline = {"bound": "hbm", "achieved": kr["achieved"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": kr["frac"], "traffic": traffic, "peak_source": peaks["source"], "kernel": kr["kernel"],
+                "kernel_us": kr["kernel_us"], "merge_us": kr["merge_us"], "append_us": kr["append_us"],
                 "copy_kernel_gbs": r["copy_gbs"],
                 "timing": "kernel events from a second pass over the same K steps"}
     cb = None if (args.no_cpu_baseline or args.quick) else cpu_baseline(w, r["mode"])
@@ -531,14 +653,19 @@ def main():
                    "kv_tokens": int(w.table.kv_len().sum()), "bytes_per_step": int(r["bytes_mean"]),
                    "l2": "flushed before every timed step, outside the timed events: 512 MB written, then "
                          "256 MB read so the step starts with a cold, clean L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": f"the timed steps are queued behind a {PREROLL_S * 1e3:.0f} ms spin kernel, so the "
+                             "host runs ahead of the GPU; garbage collection off while timing"},
         "us_per_call": ms_max * 1e3,
-        "us_p10_p50_p90": [float(np.percentile(ms, x)) * 1e3 for x in (10, 50, 90)],
+        **step_stats(ms),
+        "us_steps": [round(x * 1e3, 2) for x in ms] if len(ms) <= 64 else None,
         "rows_per_s": world * w.batch / (ms_max * 1e-3),
         "pct_of_peak": 100.0 * tbps * 1e3 / world / peaks["hbm_gbs"],
         "roofline": roofline, "cpu_baseline": cb, "e2e": r["e2e"], "gpu_launches": launches,
         "clocks": r["clocks"],
     }
+    if r["per_config"]:
+        line["per_config"] = r["per_config"]
     print(json.dumps(line))
     if world > 1:
         import torch
