@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256, 1)
     const long long pend = min(p0 + a.pos_per_warp - a.tail, a.total_pos);  // the head of share gwarp
     long long unit = a.tail ? (1 + a.tail_pieces) * gwarp : gwarp;           // unit of the chunks produced
     bool tails_left = a.tail != 0;
+    TailClaim tclaim;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
@@ -143,12 +144,8 @@ __global__ void __launch_bounds__(256, 1)
     // Emit the next chunk into `slot` (whole warp; lane 0 issues the copies).
     auto produce = [&](int slot, uint32_t extra_tx) {
         Chunk ck;
-        bool have = walk.template next<kRC>(&ck);
-        // This warp's range is done: take the next tail piece, if any is left.
-        while (!have && tails_left) {
-            tails_left = take_tail(a, walk, &unit, lane);
-            if (tails_left) have = walk.template next<kRC>(&ck);
-        }
+        // When this warp's range is done, it moves on to tail pieces (claimed ahead).
+        const bool have = next_with_tails<kRC>(a, walk, tclaim, &tails_left, &unit, kStages, lane, &ck);
         const uint32_t bar = bar0 + 8 * slot;
         uint8_t* st = wsm + slot * C::kStageBytes;
         if constexpr (kFused) {

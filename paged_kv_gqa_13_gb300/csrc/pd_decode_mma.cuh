@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(256, 1)
     const long long pend = min(p0 + ppw - a.tail, a.total_pos);  // the head of share gwarp
     long long unit = a.tail ? (1 + a.tail_pieces) * gwarp : gwarp;  // unit of the chunks being produced
     bool tails_left = a.tail != 0;
+    TailClaim tclaim;
     Walk<kFused> walk(a, s_indptr, s_lpl, p0, pend, lane);
     const int first_page = walk.prefetch_first();
     const int GT = a.heads_per_tile;
@@ -166,12 +167,8 @@ __global__ void __launch_bounds__(256, 1)
     // description is written here.
     auto produce = [&](int slot, uint32_t extra_tx, bool issued) {
         Chunk ck;
-        bool have = walk.template next<kMmaRows>(&ck);
-        // This warp's range is done: take the next tail piece, if any is left.
-        while (!have && tails_left) {
-            tails_left = take_tail(a, walk, &unit, lane);
-            if (tails_left) have = walk.template next<kMmaRows>(&ck);
-        }
+        // When this warp's range is done, it moves on to tail pieces (claimed ahead).
+        const bool have = next_with_tails<kMmaRows>(a, walk, tclaim, &tails_left, &unit, kS, lane, &ck);
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t st = wsm_u32 + slot * C::kStageBytes;
         if constexpr (kFused) {

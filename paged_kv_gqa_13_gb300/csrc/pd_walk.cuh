@@ -95,18 +95,21 @@ struct Walk {
           staged(args.table_bytes > 0), wbase(p0_), mask(0), cur(0), j(0), nxt(-1),
           e_slab(0), e_row(0), e_khf(0), e_valid(0), e_qrow(0), e_seg(0) {}
 
-    // Walk a new range [p0_, pend_) (a tail unit): its first page ids are
-    // requested and its first window described.
-    __device__ __forceinline__ void restart(long long p0_, long long pend_) {
+    // Walk a new range whose first two windows of page ids were loaded ahead
+    // (see TailClaim).
+    __device__ __forceinline__ void restart_loaded(long long p0_, long long pend_, int pg, int pg_next) {
         p0 = p0_;
         pend = pend_;
         wbase = p0_;
         cur = 0;
         j = 0;
-        const int pg = load_page(p0_ + lane);
-        nxt = load_page(p0_ + 32 + lane);
+        nxt = pg_next;
         build(p0_, pg);
     }
+
+    // Positions of the current range not emitted yet (an upper bound: some
+    // may belong to no request).
+    __device__ __forceinline__ long long left() const { return pend - (wbase + cur); }
 
     // Page id of position p (paged store), -1 outside the range.
     __device__ __forceinline__ int load_page(long long p) const {
@@ -302,28 +305,63 @@ struct Walk {
     }
 };
 
-// Dynamic tails (DecodeArgs::tail). Point `walk` at the next tail piece not
-// yet taken and set *unit to its unit; false when none is left. Called by the
-// whole warp.
-template <class W>
-__device__ __forceinline__ bool take_tail(const DecodeArgs& a, W& walk, long long* unit, int lane) {
-    const long long ppw = a.pos_per_warp;
-    const int kp = a.tail_pieces;
-    const long long n_pieces = (a.total_pos + ppw - 1) / ppw * kp;
-    const long long piece = a.tail / kp;
-    for (;;) {
-        unsigned t = 0;
-        if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
-        t = __shfl_sync(kFull, t, 0);
-        if ((long long)t >= n_pieces) return false;
-        const long long sh = (long long)t / kp, jp = (long long)t % kp;
-        const long long t0 = sh * ppw + (ppw - a.tail) + jp * piece;
-        const long long t1 = min(jp == kp - 1 ? (sh + 1) * ppw : t0 + piece, a.total_pos);
-        if (t0 >= t1) continue;  // past the last position
-        *unit = (1 + kp) * sh + 1 + jp;
-        walk.restart(t0, t1);
-        return true;
+// Dynamic tails (DecodeArgs::tail). A warp claims the next tail piece not
+// yet taken while its current range still has a few positions to go, and
+// requests that piece's first page ids at once: when the range runs out, the
+// piece's first chunk follows without waiting for the claim or the ids.
+// (Claiming only when the range had run out left each warp ~4 us without
+// data per tail on the Llama-shaped batch: the counter's round trip, the page
+// ids' round trip, then the first copy's.)
+struct TailClaim {
+    bool held = false;  // a piece is claimed and its ids requested
+    long long t0 = 0, t1 = 0, unit = 0;
+    int pg = -1, pg_next = -1;  // page ids of positions t0 + lane and t0 + 32 + lane
+
+    // Claim the next piece not yet taken; false when none is left. Called by
+    // the whole warp.
+    __device__ __forceinline__ bool claim(const DecodeArgs& a, int lane) {
+        const long long ppw = a.pos_per_warp;
+        const int kp = a.tail_pieces;
+        const long long n_pieces = (a.total_pos + ppw - 1) / ppw * kp;
+        const long long piece = a.tail / kp;
+        for (;;) {
+            unsigned t = 0;
+            if (lane == 0) t = atomicAdd(a.tail_ctl, 1u);
+            t = __shfl_sync(kFull, t, 0);
+            if ((long long)t >= n_pieces) return held = false;
+            const long long sh = (long long)t / kp, jp = (long long)t % kp;
+            t0 = sh * ppw + (ppw - a.tail) + jp * piece;
+            t1 = min(jp == kp - 1 ? (sh + 1) * ppw : t0 + piece, a.total_pos);
+            if (t0 >= t1) continue;  // past the last position
+            unit = (1 + kp) * sh + 1 + jp;
+            const bool paged = a.contiguous == 0;
+            pg = (paged && t0 + lane < t1) ? __ldg(a.indices + int((t0 + lane) % a.n_pos)) : -1;
+            pg_next = (paged && t0 + 32 + lane < t1) ? __ldg(a.indices + int((t0 + 32 + lane) % a.n_pos)) : -1;
+            return held = true;
+        }
     }
+};
+
+// The producer's next chunk, with the tails: when `walk` runs out, it moves on
+// to the claimed tail piece (setting *unit), claiming a new one while the
+// current range has at most `ahead` positions left. *tails_left turns false
+// once no piece is left to claim. Called by the whole warp.
+template <int CR, class W>
+__device__ __forceinline__ bool next_with_tails(const DecodeArgs& a, W& walk, TailClaim& tc, bool* tails_left,
+                                                long long* unit, int ahead, int lane, Chunk* ck) {
+    bool have = walk.template next<CR>(ck);
+    while (!have && *tails_left) {
+        if (!tc.held && !tc.claim(a, lane)) {
+            *tails_left = false;
+            break;
+        }
+        walk.restart_loaded(tc.t0, tc.t1, tc.pg, tc.pg_next);
+        *unit = tc.unit;
+        tc.held = false;
+        have = walk.template next<CR>(ck);
+    }
+    if (have && *tails_left && !tc.held && walk.left() <= ahead && !tc.claim(a, lane)) *tails_left = false;
+    return have;
 }
 
 // Every warp of a grid with tails calls this once, after its last chunk; the
