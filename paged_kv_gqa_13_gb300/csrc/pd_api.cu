@@ -234,8 +234,9 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->sms = di.sms;
     p->total_warps = (long long)p->ctas * p->nwarps;
     p->segments = (long long)p->head_tiles * Hk * batch;
-    // All but the E4M3 tensor-core kernel, whose two-stage ring cannot hide a
-    // tail's start (measured 36 -> 43 us on the Llama-shaped batch).
+    // All but the E4M3 tensor-core kernel: on the Llama-shaped batch its
+    // shares are ~22 positions, so a tail is one two-page stage, and tails
+    // made it slower (36 -> 43 us; with the tails claimed ahead, 36.0 -> 46.3 us).
     p->tails = p->ks.mma != 2;
     p->slots = (p->tails ? 1 + kTailMaxPieces : 1) * p->total_warps + p->segments;
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
