@@ -63,6 +63,11 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def workload_key(w, mode: str) -> str:
+    """The workload column of profiles/dram_traffic.txt: the workload's name, and its entry."""
+    return w.name + {"contiguous": "/contiguous", "contiguous_nhd": "/nhd", "paged_fp8": "/e4m3"}.get(mode, "")
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -515,7 +520,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
             tbps = tp["bytes_mean"] / (tp["ms_mean"] * 1e-3) / 1e12
             per[name] = {"workload": pc["w"].name, "mode": pc["mode"], "us_per_call": tp["ms_mean"] * 1e3,
                          **step_stats(tp["ms"]), "tbps": tbps, "pct_of_peak": 100.0 * tbps * 1e3 / peak,
-                         "bytes_per_step": int(tp["bytes_mean"]), **kr}
+                         "bytes_per_step": int(tp["bytes_mean"]), **kr,
+                         "traffic": recorded_traffic(kr["kernel"], workload_key(pc["w"], pc["mode"]))}
             del pc
             torch.cuda.empty_cache()
         out["per_config"] = per
@@ -632,8 +638,7 @@ def main():
     prof = r["prof"]
     kr = kernel_roofline({"w": w, "mode": r["mode"]}, {"prof": prof, "decode_bytes_mean": r["decode_bytes_mean"]},
                          peaks["hbm_gbs"])
-    traffic = recorded_traffic(kr["kernel"], w.name + ({"contiguous": "/contiguous", "contiguous_nhd": "/nhd",
-                                                        "paged_fp8": "/e4m3"}.get(r["mode"], "")))
+    traffic = recorded_traffic(kr["kernel"], workload_key(w, r["mode"]))
     roofline = {"bound": "hbm", "achieved": kr["achieved"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": kr["frac"], "traffic": traffic, "peak_source": peaks["source"], "kernel": kr["kernel"],
                 "kernel_us": kr["kernel_us"], "merge_us": kr["merge_us"], "append_us": kr["append_us"],
