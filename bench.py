@@ -158,6 +158,73 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(timed), "window": window}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries) every ~2 ms while the timed steps run: the timed region of one
+    workload is a few tens of milliseconds, shorter than nvidia-smi's sampling
+    period. The thread only starts once every timed step has been queued (the
+    host is waiting on the device), so it does not delay the launches."""
+
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL = 0x4, 0x8, 0x20, 0x40
+
+    def __init__(self, device_index: int):
+        import ctypes
+
+        self.samples = []
+        self.handle = None
+        try:
+            import torch
+
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            pr = torch.cuda.get_device_properties(device_index)
+            bus = b"%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                return
+            self.lib, self.handle = lib, h
+            mx = ctypes.c_uint(0)
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            self.handle = None
+
+    def _poll(self, stop):
+        import ctypes
+
+        mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0 and \
+                    self.reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            stop.wait(0.002)
+
+    def run_while(self, wait):
+        """Call wait() (a device synchronize) while sampling in a thread."""
+        if self.handle is None:
+            wait()
+            return
+        stop = threading.Event()
+        t = threading.Thread(target=self._poll, args=(stop,), daemon=True)
+        t.start()
+        try:
+            wait()
+        finally:
+            stop.set()
+            t.join()
+
+    def summary(self) -> dict | None:
+        if self.handle is None or not self.samples:
+            return None
+        names = [(self.HW_SLOWDOWN, "hw_slowdown"), (self.HW_THERMAL, "hw_thermal_slowdown"),
+                 (self.SW_THERMAL, "sw_thermal_slowdown"), (self.SW_POWER_CAP, "sw_power_cap")]
+        reasons = sorted({n for (_, r) in self.samples for (bit, n) in names if r & bit})
+        return {"sm_mhz": statistics.median(m for (m, _) in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "window": "timed region (NVML, every ~2 ms)"}
+
+
 # ---------------------------------------------------------------- workloads
 
 def load_workload(name: str, rank: int = 0):
@@ -311,7 +378,7 @@ def setup_config(args, name: str, rank: int, dev) -> dict:
     return c
 
 
-def time_steps(c, steps: int, warmup: int, flush_l2, stream, barrier=None, sampler=None) -> dict:
+def time_steps(c, steps: int, warmup: int, flush_l2, stream, barrier=None, sampler=None, nvml=None) -> dict:
     """W warm-up steps, then K timed steps (one CUDA event pair each, L2
     flushed before each outside the pair), then the same K steps again with
     the library's own events around each kernel (an event between the decode
@@ -344,7 +411,10 @@ def time_steps(c, steps: int, warmup: int, flush_l2, stream, barrier=None, sampl
             starts[i].record(stream)
             step(warmup + i)
             ends[i].record(stream)
-        torch.cuda.synchronize()
+        if nvml is not None:
+            nvml.run_while(torch.cuda.synchronize)
+        else:
+            torch.cuda.synchronize()
         if sampler is not None:
             sampler.mark("timed_end")
         if barrier is not None:
@@ -495,14 +565,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     entries = [x.strip() for x in visible.split(",") if x.strip()]
     sampler = ClockSampler(entries[local_rank] if local_rank < len(entries) else local_rank)
+    nvml = NvmlSampler(local_rank)
     barrier = torch.distributed.barrier if world > 1 else None
     t_wall = time.perf_counter()
-    t = time_steps(c, args.steps, args.warmup, flush_l2, stream, barrier, sampler)
+    t = time_steps(c, args.steps, args.warmup, flush_l2, stream, barrier, sampler, nvml)
     t_wall = time.perf_counter() - t_wall
     e2e = None
     if c["mode"] == "paged" and not c["w"].append_steps and not args.quick:
         e2e = run_e2e(c, args, dev, flush_l2, stream)
     clocks = sampler.stop()
+    timed_clocks = nvml.summary()
+    if timed_clocks is not None:
+        timed_clocks["nvidia_smi_whole_run"] = clocks
+        clocks = timed_clocks
     out = {"w": c["w"], "mode": c["mode"], "ms_mean": t["ms_mean"], "ms_all": t["ms"], "bytes_mean": t["bytes_mean"],
            "decode_bytes_mean": t["decode_bytes_mean"], "prof": t["prof"], "copy_gbs": copy_gbs, "e2e": e2e,
            "clocks": clocks, "t_wall": t_wall, "per_config": None}
