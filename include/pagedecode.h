@@ -130,7 +130,8 @@ int pd_decode_kernel_kind(int num_qo_heads, int num_kv_heads, int head_dim, pd_d
  *   be ordered on one stream.
  *
  * Long requests are split across warps in a load-balanced partition of all
- * (kv head, page) work; the last eighth of each warp's share goes, at fixed
+ * (kv head, page) work; the last part of each warp's share (a quarter of
+ * shares of up to 1,024 K/V rows, an eighth of longer ones) goes, at fixed
  * boundaries, to whichever warp finishes first (counters in the workspace
  * header, back at zero after every call). Partial (o, lse) pairs are combined
  * by a merge kernel in a fixed order, so results do not depend on timing.

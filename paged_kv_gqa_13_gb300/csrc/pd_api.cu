@@ -132,13 +132,21 @@ pd_status allow_smem(const void* fn, int bytes) {
 
 // How a decode call is laid out on the device.
 // Dynamic tails (DecodeArgs::tail): shares of at least kTailMinPos positions
-// give their last 1/kTailDiv, in kTailPieces pieces, to whichever warps
-// finish first. (Measured on GB300: 1/8 in one piece; 1/4 .. 1/6 in two
-// pieces shortened the decode of long batches by ~1% but cost more than
-// that in the merge of the 32-request batch.) The counters sit in the workspace header after the status
-// word. A plan holds 1 + kTailMaxPieces partial slots per warp.
+// give their last 1/kTailDiv (1/kTailDivShort for shares of at most
+// kShortShareRows rows), in kTailPieces pieces, to whichever warps finish
+// first; a share's length is counted in K/V rows (positions x rows per page or
+// virtual page). The counters sit in the workspace header after the status word. A
+// plan holds 1 + kTailMaxPieces partial slots per warp.
+// Measured on GB300, tails claimed ahead, same box: the 32-request Llama-shaped
+// batch (~33 pages of 16 rows per share, 528 rows) takes 64.1 / 62.4 / 62.2 us
+// per call with tails of 1/8, 1/3 and 1/4; batches with shares of ~3,000-3,500
+// rows (ragged 70B, long context paged and contiguous, MHA) are fastest at 1/8
+// and lose 2.5-5 % at 1/5 or 1/4. Earlier, tails of 1/4 .. 1/6 cut in two pieces shortened the long
+// batches by ~1 % but cost more than that in the merge of the 32-request batch.
 constexpr long long kTailMinPos = 12;
 constexpr long long kTailDiv = 8;
+constexpr long long kShortShareRows = 1024;
+constexpr long long kTailDivShort = 4;
 constexpr int kTailPieces = 1;
 constexpr int kTailMaxPieces = 1;
 constexpr size_t kTailCtlOff = 64;
@@ -381,10 +389,11 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
             grid = int((warps_used + pl.nwarps - 1) / pl.nwarps);
         }
         // SMs stream at different rates (by up to ~25% across one GPU), so
-        // equal shares end at different times: the last kTailDiv-th of each
-        // share is handed out to the warps that finish first.
+        // equal shares end at different times: the last part of each share is
+        // handed out to the warps that finish first.
         if (pl.tails && a.pos_per_warp >= kTailMinPos) {
-            a.tail = int(a.pos_per_warp / kTailDiv);
+            const long long share_rows = a.pos_per_warp * (a.contiguous ? a.vpage : a.page_size);
+            a.tail = int(a.pos_per_warp / (share_rows <= kShortShareRows ? kTailDivShort : kTailDiv));
             a.tail_pieces = a.tail >= kTailPieces ? kTailPieces : 1;
             a.tail_ctl = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(a.flags) + kTailCtlOff);
         }
