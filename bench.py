@@ -529,6 +529,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
+    pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TCGEN05 if args.fp8_kernel == "tcgen05" else pd.PD_KERNEL_FP8_TENSOR_CORES)
     c = setup_config(args, args.config, rank, dev)
 
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -668,6 +669,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--append", default="fused", choices=["fused", "separate"],
                     help="append workloads: one fused append + decode launch, or an append launch then a decode")
+    ap.add_argument("--fp8-kernel", default="mma", choices=["mma", "tcgen05"],
+                    help="E4M3 pools: the mma.sync kernel (default) or the tcgen05 one where it applies")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="skip the extra workloads timed after the headline one (one GPU only)")
@@ -727,7 +730,8 @@ def main():
         "metric": METRIC, "value": tbps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if r["mode"] == "paged_fp8" else w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "mode": r["mode"] + (f", append {args.append}" if w.append_steps else ""),
+        "config": {"workload": w.name, "mode": r["mode"] + (f", append {args.append}" if w.append_steps else "")
+                   + (", tcgen05 kernel" if r["mode"] == "paged_fp8" and args.fp8_kernel == "tcgen05" else ""),
                    "batch": w.batch, "num_qo_heads": w.num_qo_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
                    "kv_tokens": int(w.table.kv_len().sum()), "bytes_per_step": int(r["bytes_mean"]),

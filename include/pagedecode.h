@@ -100,7 +100,10 @@ size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_h
  * is served in tiles of at most 8 q heads, padded to 1, 2, 4 or 8. 16-bit
  * tiles of 4 or 8 run on tensor cores; f32 and 16-bit tiles of 1 or 2 run on
  * CUDA cores. Over E4M3 pools, tiles of 4 or 8 at head_dim 128 or 256 run on
- * the E4M3 tensor-core kernel, the rest on CUDA cores. This is a host-side
+ * the mma.sync E4M3 tensor-core kernel, or, when pd_select_fp8_kernel chose
+ * it and the shape allows it (bf16 q, groups of exactly 4 q heads, an even
+ * number of kv heads, head_dim 128), on the tcgen05 kernel; the rest run on
+ * CUDA cores. This is a host-side
  * lookup: it needs no device, enqueues nothing and returns PD_KERNEL_NONE for
  * a shape that no call accepts.
  */
@@ -108,7 +111,21 @@ size_t pd_paged_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_h
 #define PD_KERNEL_CUDA_CORES 1
 #define PD_KERNEL_TENSOR_CORES 2
 #define PD_KERNEL_FP8_TENSOR_CORES 3
+#define PD_KERNEL_FP8_TCGEN05 4
 int pd_decode_kernel_kind(int num_qo_heads, int num_kv_heads, int head_dim, pd_dtype dtype, int fp8_pool);
+
+/*
+ * Which tensor-core kernel decodes over E4M3 pools where both apply (bf16 q,
+ * groups of exactly 4 q heads, an even number of kv heads, head_dim 128):
+ * PD_KERNEL_FP8_TENSOR_CORES (mma.sync over codes widened in registers; the
+ * default, and the faster on the measured shapes) or PD_KERNEL_FP8_TCGEN05
+ * (tcgen05.mma on the codes in shared memory, accumulators in tensor memory).
+ * Both give results within the same tolerances. Process-wide; it applies to
+ * the calls made after it returns, and to pd_decode_kernel_kind and the
+ * workspace sizes (which may differ between the two). PD_ERR_INVALID for any
+ * other value.
+ */
+pd_status pd_select_fp8_kernel(int kind);
 
 /*
  * Batched paged decode (batch_paged_decode.rs: BatchPagedDecodePlan::run and

@@ -31,6 +31,7 @@ PD_OK, PD_ERR_INVALID, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA = 0, 1,
 PD_FLAG_BAD_PAGE_ID, PD_FLAG_BAD_LAST_PAGE_LEN, PD_FLAG_BAD_INDPTR, PD_FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 PD_WORKSPACE_HEADER_BYTES = 256
 PD_KERNEL_NONE, PD_KERNEL_CUDA_CORES, PD_KERNEL_TENSOR_CORES, PD_KERNEL_FP8_TENSOR_CORES = 0, 1, 2, 3
+PD_KERNEL_FP8_TCGEN05 = 4
 
 STATUS_NAMES = {0: "PD_OK", 1: "PD_ERR_INVALID", 2: "PD_ERR_UNSUPPORTED", 3: "PD_ERR_WORKSPACE",
                 4: "PD_ERR_CUDA"}
@@ -49,6 +50,7 @@ _SIGS = {
     "pd_copy_bytes": (_I, [_P, _P, _S, _P]),
     "pd_profile_enable": (_I, [_I]),
     "pd_test_inject_wait_timeout": (_I, [_I]),
+    "pd_select_fp8_kernel": (_I, [_I]),
     "pd_profile_read": (_I, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
@@ -340,6 +342,11 @@ def pd_paged_append_fp8(k_new, v_new, k_scale, v_scale, k_data, v_data, indices,
         _ptr(indices) if indices.numel() else None, _ptr(indptr), _ptr(last_page_len), batch, num_kv_heads,
         head_dim, page_size, num_total_pages, indices.numel(), _dtype_code(k_new), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+
+
+def pd_select_fp8_kernel(kind: int) -> None:
+    """Choose PD_KERNEL_FP8_TENSOR_CORES (default) or PD_KERNEL_FP8_TCGEN05 for E4M3 pools where both apply."""
+    _check(_lib.pd_select_fp8_kernel(int(kind)))
 
 
 def pd_test_inject_wait_timeout(extra_bytes: int) -> None:

@@ -26,8 +26,8 @@ PD_VARIANTS(f32)
 PD_VARIANTS(f16)
 PD_VARIANTS(bf16)
 #undef PD_VARIANTS
-bool lookup_fp8_f16(int head_dim, int heads, KernelSet* ks);
-bool lookup_fp8_bf16(int head_dim, int heads, KernelSet* ks);
+bool lookup_fp8_f16(int head_dim, int heads, bool kv_pairs, KernelSet* ks);
+bool lookup_fp8_bf16(int head_dim, int heads, bool kv_pairs, KernelSet* ks);
 }  // namespace pd
 
 namespace {
@@ -72,10 +72,19 @@ bool lookup(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
 }
 
 // Kernels for an E4M3 pool with q / o of type dt (f16 or bf16).
-bool lookup_fp8(pd_dtype dt, int D, int G, pd::KernelSet* ks) {
+// pd_select_fp8_kernel: 1 when the tcgen05 E4M3 kernel is chosen where it applies.
+std::atomic<int> g_fp8_tcgen05{0};
+
+bool kv_pairs_ok(pd_dtype dt, int Hq, int Hk) {
+    return g_fp8_tcgen05.load(std::memory_order_relaxed) != 0 && dt == PD_BF16 && Hk % 2 == 0 && Hq == 4 * Hk;
+}
+
+// kv_pairs: the shape allows the kernel that takes the kv heads in pairs (bf16,
+// groups of exactly 4 q heads, an even number of kv heads).
+bool lookup_fp8(pd_dtype dt, int D, int G, bool kv_pairs, pd::KernelSet* ks) {
     switch (dt) {
-        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fp8_f16(D, G, ks);
-        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fp8_bf16(D, G, ks);
+        case PD_F16: return pd::lookup_kernels_f16(D, G, ks) && pd::lookup_fp8_f16(D, G, kv_pairs, ks);
+        case PD_BF16: return pd::lookup_kernels_bf16(D, G, ks) && pd::lookup_fp8_bf16(D, G, kv_pairs, ks);
         default: return false;
     }
 }
@@ -156,9 +165,14 @@ struct Plan {
     pd::KernelSet ks{};
     int table_bytes = 0, nwarps = 0, ctas = 0, sms = 0;
     long long total_warps = 0, segments = 0, slots = 0;
+    int walk_kv = 0;     // kv heads as the walk and the merge see them: Hk, or Hk / 2 pairs (ks.mma 3)
     bool tails = false;  // the decode kernel takes DecodeArgs::tail (slots for two units per warp)
     size_t smem = 0, lse_off = 0, o_off = 0, ws_bytes = 0;
 };
+
+// Threads per decode block: one warp per share, or the kernel's own block
+// when its shares are groups of warps.
+int block_threads(const Plan& p) { return p.ks.threads > 0 ? p.ks.threads : p.nwarps * 32; }
 
 // Smallest number of head tiles that splits the group into tiles of <= 8 heads.
 void split_group(int g, int* tiles, int* per) {
@@ -178,19 +192,20 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
         int dev;
         pd_dtype dt;
         int batch, Hq, Hk, D;
-        bool contiguous, fp8;
+        bool contiguous, fp8, tcgen05;
         Plan plan;
     };
     static Entry cache[16];
     static int used = 0, next = 0;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    const bool tcgen05 = g_fp8_tcgen05.load(std::memory_order_relaxed) != 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int i = 0; i < used; ++i) {
             const Entry& e = cache[i];
             if (e.dev == dev && e.dt == dt && e.batch == batch && e.Hq == Hq && e.Hk == Hk && e.D == D &&
-                e.contiguous == contiguous && e.fp8 == fp8) {
+                e.contiguous == contiguous && e.fp8 == fp8 && e.tcgen05 == tcgen05) {
                 *p = e.plan;
                 return PD_OK;
             }
@@ -199,7 +214,7 @@ pd_status make_plan(pd_dtype dt, int batch, int Hq, int Hk, int D, bool contiguo
     const pd_status st = make_plan_uncached(dt, batch, Hq, Hk, D, contiguous, fp8, p);
     if (st != PD_OK) return st;
     std::lock_guard<std::mutex> lk(g_mu);
-    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, fp8, *p};
+    cache[next] = Entry{dev, dt, batch, Hq, Hk, D, contiguous, fp8, tcgen05, *p};
     next = (next + 1) % 16;
     if (used < 16) ++used;
     return PD_OK;
@@ -215,16 +230,24 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->G = 1;
     while (p->G < p->heads_per_tile) p->G *= 2;
     if (fp8 && dt == PD_F32) return fail(PD_ERR_UNSUPPORTED, "E4M3 pools take f16 or bf16 q and o");
-    if (!(fp8 ? lookup_fp8(dt, D, p->G, &p->ks) : lookup(dt, D, p->G, &p->ks)))
+    if (!(fp8 ? lookup_fp8(dt, D, p->G, kv_pairs_ok(dt, Hq, Hk), &p->ks) : lookup(dt, D, p->G, &p->ks)))
         return fail(PD_ERR_UNSUPPORTED, "no kernel for head_dim %d, %d heads per tile", D, p->G);
     p->G = p->ks.part_heads;  // the partial-result layout of the chosen kernel
+    p->walk_kv = Hk;
+    if (p->ks.mma == 3) {
+        // kv heads in pairs: a pair and its 8 q heads are one kv head of group 8
+        p->walk_kv = Hk / 2;
+        p->group *= 2;
+        p->heads_per_tile *= 2;
+    }
     DeviceInfo di;
     pd_status st = device_info(&di);
     if (st != PD_OK) return st;
     p->table_bytes = pd::table_bytes_for(!contiguous && batch <= pd::kTableMax);
     p->nwarps = (di.max_smem - p->table_bytes - p->ks.smem_slack) / p->ks.warp_bytes;
     if (p->nwarps > p->ks.max_warps) p->nwarps = p->ks.max_warps;
-    if (p->nwarps < 1) return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
+    if (p->nwarps < 1 || (p->ks.threads > 0 && p->nwarps != p->ks.max_warps))
+        return fail(PD_ERR_UNSUPPORTED, "shared memory per block too small for this shape");
     p->smem = size_t(p->ks.smem_slack) + size_t(p->table_bytes) + size_t(p->nwarps) * p->ks.warp_bytes;
     // The variants this plan may launch (NHD only on the contiguous cache) all
     // share its layout; size one wave by the lowest of their occupancies.
@@ -233,7 +256,7 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
         if (p->ks.variant[v] == nullptr) continue;
         if ((st = allow_smem(p->ks.variant[v], int(p->smem))) != PD_OK) return st;
         int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, p->ks.variant[v], p->nwarps * 32, p->smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, p->ks.variant[v], block_threads(*p), p->smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (n < per_sm) per_sm = n;
     }
@@ -241,11 +264,12 @@ pd_status make_plan_uncached(pd_dtype dt, int batch, int Hq, int Hk, int D, bool
     p->ctas = di.sms * per_sm;
     p->sms = di.sms;
     p->total_warps = (long long)p->ctas * p->nwarps;
-    p->segments = (long long)p->head_tiles * Hk * batch;
-    // All but the E4M3 tensor-core kernel: on the Llama-shaped batch its
-    // shares are ~22 positions, so a tail is one two-page stage, and tails
-    // made it slower (36 -> 43 us; with the tails claimed ahead, 36.0 -> 46.3 us).
-    p->tails = p->ks.mma != 2;
+    p->segments = (long long)p->head_tiles * p->walk_kv * batch;
+    // All but the E4M3 tensor-core kernels: on the Llama-shaped batch the
+    // mma.sync one's shares are ~22 positions, so a tail is one two-page
+    // stage, and tails made it slower (36 -> 43 us; with the tails claimed
+    // ahead, 36.0 -> 46.3 us); the tcgen05 one has one share per block.
+    p->tails = p->ks.mma < 2;
     p->slots = (p->tails ? 1 + kTailMaxPieces : 1) * p->total_warps + p->segments;
     p->lse_off = PD_WORKSPACE_HEADER_BYTES;
     p->o_off = p->lse_off + (size_t(p->slots) * p->G * 4 + 255) / 256 * 256;
@@ -281,7 +305,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // head_dim columns x `box_rows` rows (the CUDA-core kernel on an NHD cache).
 // A box holds rows of one kv head, so it lands as consecutive rows either way.
 pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, long long rows, long long slab_rows,
-                      int Hk, long long slabs, bool nhd, int mma, int box_rows) {
+                      int Hk, long long slabs, bool nhd, int mma, int box_rows, int box_heads = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     // mma 2: E4M3 codes, one byte per element, whatever the type of q and o
@@ -295,7 +319,7 @@ pd_status make_kv_map(CUtensorMap* map, const void* base, pd_dtype dt, int D, lo
     // a swizzled box row is 128 bytes: 64 16-bit or 128 E4M3 elements
     const cuuint32_t cols = mma == 2 ? 128u : mma ? 64u : cuuint32_t(D);
     const cuuint32_t brows = mma ? cuuint32_t(pd::kMmaRows) : cuuint32_t(box_rows);
-    const cuuint32_t box_hnd[4] = {cols, brows, 1, 1};
+    const cuuint32_t box_hnd[4] = {cols, brows, cuuint32_t(box_heads), 1};
     const cuuint32_t box_nhd[4] = {cols, 1, brows, 1};
     const cuuint32_t* box = nhd ? box_nhd : box_hnd;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -357,12 +381,14 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     std::memset(maps, 0, sizeof(maps));
     if ((pl.ks.mma || nhd) && a.total_pos > 0) {
         const long long rows = a.contiguous ? a.valid_kv_len : a.slab_rows;
-        const int mma = pl.ks.mma;
+        // both E4M3 kernels take 128-code boxes; the tcgen05 one two kv heads per box
+        const int mma = pl.ks.mma == 3 ? 2 : pl.ks.mma;
+        const int box_heads = pl.ks.mma == 3 ? 2 : 1;
         pd_status st = make_kv_map(&maps[0], a.k, dt, D, rows, a.slab_rows, a.num_kv_heads, slabs, nhd, mma,
-                                   pl.ks.rows_per_stage);
+                                   pl.ks.rows_per_stage, box_heads);
         if (st == PD_OK)
             st = make_kv_map(&maps[1], a.v, dt, D, rows, a.slab_rows, a.num_kv_heads, slabs, nhd, mma,
-                             pl.ks.rows_per_stage);
+                             pl.ks.rows_per_stage, box_heads);
         if (st != PD_OK) return st;
     }
     std::unique_lock<std::mutex> plk(g_prof_mu);
@@ -399,7 +425,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
         }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(pl.nwarps * 32);
+        cfg.blockDim = dim3(block_threads(pl));
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = stream;
         void* args[] = {&a, &maps[0], &maps[1]};
@@ -419,7 +445,7 @@ pd_status launch_decode(const Plan& pl, pd::DecodeArgs& a, int D, pd_dtype dt, l
     m.flags = a.flags;
     m.batch = a.batch;
     m.num_qo_heads = a.num_qo_heads;
-    m.num_kv_heads = a.num_kv_heads;
+    m.num_kv_heads = pl.walk_kv;
     m.group = a.group;
     m.head_tiles = a.head_tiles;
     m.heads_per_tile = a.heads_per_tile;
@@ -604,8 +630,13 @@ int pd_decode_kernel_kind(int num_qo_heads, int num_kv_heads, int head_dim, pd_d
     int G = 1;
     while (G < per) G *= 2;
     pd::KernelSet ks{};
-    if (!(fp8_pool ? lookup_fp8(dtype, head_dim, G, &ks) : lookup(dtype, head_dim, G, &ks))) return PD_KERNEL_NONE;
-    return ks.mma == 2 ? PD_KERNEL_FP8_TENSOR_CORES : ks.mma == 1 ? PD_KERNEL_TENSOR_CORES : PD_KERNEL_CUDA_CORES;
+    if (!(fp8_pool ? lookup_fp8(dtype, head_dim, G, kv_pairs_ok(dtype, num_qo_heads, num_kv_heads), &ks)
+                   : lookup(dtype, head_dim, G, &ks)))
+        return PD_KERNEL_NONE;
+    return ks.mma == 3   ? PD_KERNEL_FP8_TCGEN05
+           : ks.mma == 2 ? PD_KERNEL_FP8_TENSOR_CORES
+           : ks.mma == 1 ? PD_KERNEL_TENSOR_CORES
+                         : PD_KERNEL_CUDA_CORES;
 }
 
 size_t pd_contiguous_decode_workspace_bytes(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
@@ -670,7 +701,7 @@ static pd_status paged_decode_impl(const void* q, const void* k_new, const void*
     a.heads_per_tile = pl.heads_per_tile;
     a.n_pos = num_indices;
     a.table_bytes = pl.table_bytes;
-    a.total_pos = (long long)pl.head_tiles * num_kv_heads * num_indices;
+    a.total_pos = (long long)pl.head_tiles * pl.walk_kv * num_indices;
     a.q_scale = sm_scale * pd::kLog2e;
     a.contiguous = 0;
     a.slab_rows = page_size;
@@ -999,6 +1030,13 @@ pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream) 
         static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+    return ok();
+}
+
+pd_status pd_select_fp8_kernel(int kind) {
+    if (kind != PD_KERNEL_FP8_TENSOR_CORES && kind != PD_KERNEL_FP8_TCGEN05)
+        return fail(PD_ERR_INVALID, "kind must be PD_KERNEL_FP8_TENSOR_CORES or PD_KERNEL_FP8_TCGEN05");
+    g_fp8_tcgen05.store(kind == PD_KERNEL_FP8_TCGEN05 ? 1 : 0, std::memory_order_relaxed);
     return ok();
 }
 

@@ -6,6 +6,7 @@
 #include "pd_decode.cuh"
 #include "pd_decode_fp8.cuh"
 #include "pd_decode_mma.cuh"
+#include "pd_decode_tc.cuh"
 #include "pd_merge.cuh"
 
 namespace pd {
@@ -19,10 +20,13 @@ struct KernelSet {
     const void* merge_states;
     int warp_bytes;      // dynamic shared memory per decode warp
     int rows_per_stage;  // K (and V) rows one pipeline stage holds
-    int mma;             // K/V copies through 128B-swizzled tensor maps: 1 16-bit pools, 2 E4M3 pools (tensor cores)
+    int mma;             // K/V copies through 128B-swizzled tensor maps: 1 16-bit pools, 2 E4M3 pools (tensor
+                         // cores), 3 E4M3 pools (tcgen05, one share per block)
     int part_heads;      // heads per partial-result slot: the group tile G, or 8 for the tensor-core kernel
     int smem_slack;      // extra dynamic shared memory for aligning the stages
-    int max_warps;       // warps per block the kernel is built for (its launch bound / 32)
+    int max_warps;       // shares per block the kernel is built for (one per warp unless `threads` is set)
+    int threads;         // threads per block of a kernel whose shares are groups of warps (0: a warp per share);
+                         // it then runs exactly max_warps shares per block
 };
 
 // Kernels and sizes for (T, head_dim, heads per tile): 16-bit tiles of 4 to
@@ -40,6 +44,7 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
         ks->part_heads = 8;                                                             \
         ks->smem_slack = 1024;                                                          \
         ks->max_warps = 8;                                                              \
+        ks->threads = 0;                                                                \
     }
 #define PD_CC(DD, GG)                                                                   \
     {                                                                                   \
@@ -50,6 +55,7 @@ bool lookup_kernels_t(int D, int G, KernelSet* ks) {
         ks->part_heads = GG;                                                            \
         ks->smem_slack = 0;                                                             \
         ks->max_warps = 8;                                                              \
+        ks->threads = 0;                                                                \
     }
 #define PD_CASE(DD, GG)                                                                 \
     if (D == DD && G == GG) {                                                           \
@@ -94,17 +100,38 @@ bool lookup_variant_t(int D, int G, const void** fn) {
     return false;
 }
 
-// The decode kernel for E4M3 pools with q / o of type T (16-bit). Tiles of 4
-// or more q heads at head_dim 128 / 256 go to the tensor-core kernel (the
-// CUDA cores would be issue-bound there: an E4M3 byte is a whole element);
-// the rest to the CUDA-core kernel. The merge kernels are those of T (from
+// The tcgen05 E4M3 kernel for bf16 q / o (null for f16, which it does not take).
+template <typename T>
+const void* tc_fp8_kernel() {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return reinterpret_cast<const void*>(decode_tc_fp8_kernel<T>);
+    else
+        return nullptr;
+}
+
+// The decode kernel for E4M3 pools with q / o of type T (16-bit). kv_pairs
+// (bf16, groups of exactly 4 q heads, an even number of kv heads): head_dim 128
+// goes to the tcgen05 kernel, which takes the kv heads in pairs. Other tiles of
+// 4 or more q heads at head_dim 128 / 256 go to the mma.sync tensor-core kernel
+// (the CUDA cores would be issue-bound there: an E4M3 byte is a whole
+// element); the rest to the CUDA-core kernel. The merge kernels are those of T (from
 // lookup_kernels_t), left untouched here.
 template <typename T>
-bool lookup_fp8_t(int D, int G, KernelSet* ks) {
+bool lookup_fp8_t(int D, int G, bool kv_pairs, KernelSet* ks) {
     static_assert(sizeof(T) == 2, "E4M3 pools take 16-bit q / o");
 #define PD_CASE(DD, GG)                                                                      \
     if (D == DD && G == GG) {                                                                \
-        if constexpr (DD >= 128 && GG >= 4) {                                                \
+        ks->threads = 0;                                                                     \
+        if (std::is_same<T, __nv_bfloat16>::value && DD == 128 && GG == 4 && kv_pairs) {     \
+            ks->decode = reinterpret_cast<const void*>(tc_fp8_kernel<T>());                   \
+            ks->warp_bytes = CfgTc::kPipeBytes;                                              \
+            ks->rows_per_stage = kMmaRows;                                                   \
+            ks->part_heads = 8;                                                              \
+            ks->smem_slack = 1024;                                                           \
+            ks->max_warps = CfgTc::kPipes;                                                   \
+            ks->threads = CfgTc::kThreads;                                                   \
+            ks->mma = 3;                                                                     \
+        } else if constexpr (DD >= 128 && GG >= 4) {                                         \
             ks->decode = reinterpret_cast<const void*>(decode_fp8_mma_kernel<T, DD>);        \
             ks->warp_bytes = CfgF8<DD>::kWarpBytes;                                          \
             ks->rows_per_stage = kMmaRows;                                                   \

@@ -264,15 +264,14 @@ struct Walk {
     }
 
     // The next chunk of at most CR rows; false when the range is exhausted.
-    template <int CR>
-    __device__ __forceinline__ bool next(Chunk* ck) {
-        bool have = false;
+    // Move `cur` to the next lane whose position belongs to a request,
+    // describing further windows as needed; false when the range is exhausted.
+    __device__ __forceinline__ bool seek() {
         while (wbase < pend) {
             const unsigned rest = cur < 32 ? (mask >> cur) : 0u;
             if (rest != 0u) {
                 cur += __ffs(rest) - 1;
-                have = true;
-                break;
+                return true;
             }
             wbase += 32;
             cur = 0;
@@ -282,7 +281,12 @@ struct Walk {
             nxt = load_page(wbase + 32 + lane);
             build(wbase, pg);
         }
-        if (!have) return false;
+        return false;
+    }
+
+    template <int CR>
+    __device__ __forceinline__ bool next(Chunk* ck) {
+        if (!seek()) return false;
         const int valid = __shfl_sync(kFull, e_valid, cur);
         const int khf = __shfl_sync(kFull, e_khf, cur);
         ck->slab = __shfl_sync(kFull, e_slab, cur);

@@ -128,10 +128,12 @@ def test_a_c_program_compiles_links_and_runs_against_the_header(tmp_path):
     assert out == [str(len(names)), "1", "str"]
 
 
-def _expected_kind(hq, hk, d, dtype, fp8):
+def _expected_kind(hq, hk, d, dtype, fp8, tcgen05=False):
     """The dispatch rule, written out: the group is cut into the fewest equal
     tiles of at most 8 heads, padded to 1, 2, 4 or 8; 16-bit tiles of 4 or 8
-    run on tensor cores; over E4M3 pools only at head_dim 128 or 256."""
+    run on tensor cores; over E4M3 pools only at head_dim 128 or 256, and, when
+    the tcgen05 kernel is selected, with bf16 q, groups of exactly 4 and an
+    even number of kv heads at head_dim 128 on that kernel."""
     import paged_kv_gqa_13_gb300 as pd
 
     if hq <= 0 or hk <= 0 or hq % hk or d not in (64, 128, 256) or (fp8 and dtype == pd.PD_F32):
@@ -140,6 +142,8 @@ def _expected_kind(hq, hk, d, dtype, fp8):
     tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
     pad = 1 << (g // tiles - 1).bit_length()
     if fp8:
+        if tcgen05 and d == 128 and dtype == pd.PD_BF16 and g == 4 and hk % 2 == 0:
+            return pd.PD_KERNEL_FP8_TCGEN05
         return pd.PD_KERNEL_FP8_TENSOR_CORES if (d >= 128 and pad >= 4) else pd.PD_KERNEL_CUDA_CORES
     return pd.PD_KERNEL_TENSOR_CORES if (dtype != pd.PD_F32 and pad >= 4) else pd.PD_KERNEL_CUDA_CORES
 
@@ -167,3 +171,32 @@ def test_decode_kernel_kind_follows_the_dispatch_rule():
                     for fp8 in (False, True):
                         assert k(g * hk, hk, d, dtype, fp8) == _expected_kind(g * hk, hk, d, dtype, fp8), \
                             (g, hk, d, dtype, fp8)
+
+
+def test_fp8_kernel_selection_changes_the_dispatch_only_where_both_kernels_apply():
+    """pd_select_fp8_kernel picks the tcgen05 E4M3 kernel for bf16 q, groups of
+    exactly 4, an even number of kv heads and head_dim 128; every other shape
+    keeps its kernel. Host-side only."""
+    import paged_kv_gqa_13_gb300 as pd
+
+    k = pd.pd_decode_kernel_kind
+    try:
+        pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TCGEN05)
+        assert k(32, 8, 128, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TCGEN05      # Llama-3-8B shape
+        assert k(64, 8, 128, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES  # group 8
+        assert k(32, 8, 128, pd.PD_F16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES   # f16 q
+        assert k(12, 3, 128, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES  # odd number of kv heads
+        assert k(32, 8, 256, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES  # head_dim 256
+        assert k(32, 8, 128, pd.PD_BF16) == pd.PD_KERNEL_TENSOR_CORES            # 16-bit pools unchanged
+        for dtype in (pd.PD_F16, pd.PD_BF16):
+            for d in (64, 128, 256):
+                for hk in (1, 2, 3, 8):
+                    for g in range(1, 13):
+                        for fp8 in (False, True):
+                            assert k(g * hk, hk, d, dtype, fp8) == _expected_kind(g * hk, hk, d, dtype, fp8, True), \
+                                (g, hk, d, dtype, fp8)
+        with pytest.raises(pd.PagedecodeError):
+            pd.pd_select_fp8_kernel(pd.PD_KERNEL_TENSOR_CORES)
+    finally:
+        pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TENSOR_CORES)
+    assert k(32, 8, 128, pd.PD_BF16, True) == pd.PD_KERNEL_FP8_TENSOR_CORES
