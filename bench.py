@@ -43,7 +43,7 @@ DEFAULT_CONFIG = "llama3_8b"
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["paged_kv_gqa_13_gb300/csrc/" + f for f in
                   ("pd_device.cuh", "pd_walk.cuh", "pd_decode.cuh", "pd_decode_mma.cuh", "pd_decode_fp8.cuh",
-                   "pd_merge.cuh")]
+                   "pd_decode_tc.cuh", "pd_merge.cuh")]
 
 
 def kernel_sha() -> str:
@@ -240,15 +240,15 @@ def load_workload(name: str, rank: int = 0):
 
 
 def decode_kernel_name(w, mode: str = "paged") -> str:
-    """The decode kernel the library picks for this workload: tensor cores for
-    16-bit tiles of 4..8 q heads per kv head, CUDA cores otherwise; for E4M3
-    pools, tensor cores for tiles of 4..8 at head_dim 128 / 256."""
-    g = w.group
-    tiles = next(t for t in range(1, g + 1) if g % t == 0 and g // t <= 8)
-    pad = 1 << (g // tiles - 1).bit_length()
-    if mode == "paged_fp8":
-        return "decode_fp8_mma_kernel" if (w.head_dim >= 128 and pad >= 4) else "decode_kernel"
-    return "decode_mma_kernel" if (w.dtype != "f32" and pad >= 4) else "decode_kernel"
+    """The decode kernel the library runs for this workload (its own host-side
+    lookup, pd_decode_kernel_kind)."""
+    import paged_kv_gqa_13_gb300 as pd
+
+    code = {"f32": pd.PD_F32, "f16": pd.PD_F16, "bf16": pd.PD_BF16}[w.dtype]
+    kind = pd.pd_decode_kernel_kind(w.num_qo_heads, w.num_kv_heads, w.head_dim, code, mode == "paged_fp8")
+    return {pd.PD_KERNEL_CUDA_CORES: "decode_kernel", pd.PD_KERNEL_TENSOR_CORES: "decode_mma_kernel",
+            pd.PD_KERNEL_FP8_TENSOR_CORES: "decode_fp8_mma_kernel",
+            pd.PD_KERNEL_FP8_TCGEN05: "decode_tc_fp8_kernel"}[kind]
 
 
 def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:
