@@ -26,9 +26,13 @@
 //    contiguous codes per token row and pairs the tokens' bytes with byte
 //    permutes; o is written back through the same map. No shared-memory
 //    tile is written, which leaves room for a third pipeline stage;
-//  - keeps q in f16 as a high and a low part of q * sm_scale * log2 e *
-//    k_scale (q ~ hi + lo to ~2^-22 relative), and P in f16 alone (V is
-//    exact in f16, so P's rounding costs o no more than its own f16 rounding). q is not staged with the pages:
+//  - keeps q in f16 as q 2^-e, e a power of two per head that puts its
+//    largest |q| into [2^14, 2^15): a bf16 or f16 q is then exact in f16 (an
+//    element more than 2^28 below the largest keeps an error under 2^-24 of
+//    it), one mma per k step forms the dot products, and 2^e, sm_scale,
+//    log2 e and k_scale multiply the f32 sums. P enters in f16 alone (V is
+//    exact in f16, so P's rounding costs o no more than its own f16
+//    rounding). q is not staged with the pages:
 //    the producer pulls a segment's q rows into L2 with its first stage, and
 //    the consumer loads its fragments from there, which keeps a warp's shared
 //    memory to its two stages of codes.
@@ -167,7 +171,8 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
 
     // ---- consumer state: lane (g, c) owns tokens g, g+8 of each tile and heads 2c, 2c+1
     const int g = lane >> 2, c = lane & 3;
-    uint32_t qh[kKS][2], ql[kKS][2];  // score-mma B fragments (permuted dims), high and low f16 parts
+    uint32_t qh[kKS][2];  // score-mma B fragments (permuted dims): q 2^-e in f16, exact
+    float qsc0 = 0.f, qsc1 = 0.f;  // 2^e * sm_scale * log2 e * k_scale of heads 2c and 2c + 1
     float acc[kKS][4];  // P.V accumulators: o^T[v_dim(mt, 0 / 1)][head 2c (+1)]
     // The dim that accumulator row g (hi = 0) or g + 8 (hi = 1) of m tile mt stands for.
     auto v_dim = [&](int mt, int hi) { return 64 * (mt >> 2) + 32 * hi + 4 * g + (mt & 3); };
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     };
     reset_state();
 #pragma unroll
-    for (int kk = 0; kk < kKS; ++kk) qh[kk][0] = qh[kk][1] = ql[kk][0] = ql[kk][1] = 0u;
+    for (int kk = 0; kk < kKS; ++kk) qh[kk][0] = qh[kk][1] = 0u;
 
     auto finalize = [&](int4 m) {
 #pragma unroll
@@ -242,35 +247,45 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         const int rows[2] = {m.x & 0xffff, m.x >> 16};
         if (m.y & kSegStart) {
             // q of head g at the permuted dims of k step kk = 4j + t:
-            // k_base(c, j) + 4t + {0, 1} (first register), + {2, 3} (second).
+            // k_base(c, j) + 4t + {0, 1} (first register), + {2, 3} (second),
+            // scaled by a power of two 2^-e (the head's largest |q| into
+            // [2^14, 2^15)): a bf16 or f16 q is then exact in f16, and 2^e and
+            // the scales multiply the f32 sums.
             const float qs = a.q_scale * __ldg(a.k_scale + (m.z % a.num_qo_heads) / a.group);
             const uint8_t* qb = static_cast<const uint8_t*>(a.q) + (size_t(m.z) + g) * q_row_bytes;
+            uint2 w[kKS];
+            float mx = 0.f;
 #pragma unroll
             for (int kk = 0; kk < kKS; ++kk) {
                 const int j = kk >> 2;
                 const int d0 = 128 * (j >> 1) + 32 * c + 16 * (j & 1) + 4 * (kk & 3);
-                uint2 w = make_uint2(0u, 0u);
-                if (g < GT) w = __ldg(reinterpret_cast<const uint2*>(qb + d0 * 2));
-                const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float2 v = unpack_pair<T>(ww[hf]);
-                    v.x *= qs;
-                    v.y *= qs;
-                    qh[kk][hf] = pack_pair<M>(v.x, v.y);
-                    const float2 r = unpack_pair<M>(qh[kk][hf]);
-                    ql[kk][hf] = pack_pair<M>(v.x - r.x, v.y - r.y);
-                }
+                w[kk] = make_uint2(0u, 0u);
+                if (g < GT) w[kk] = __ldg(reinterpret_cast<const uint2*>(qb + d0 * 2));
+                const float2 v0 = unpack_pair<T>(w[kk].x), v1 = unpack_pair<T>(w[kk].y);
+                mx = fmaxf(fmaxf(mx, fmaxf(fabsf(v0.x), fabsf(v0.y))), fmaxf(fabsf(v1.x), fabsf(v1.y)));
             }
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+            const int e = mx > 0.f ? max(-100, min(100, ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14)) : 0;
+            const float inv = __int_as_float((127 - e) << 23);
+#pragma unroll
+            for (int kk = 0; kk < kKS; ++kk) {
+                const float2 v0 = unpack_pair<T>(w[kk].x), v1 = unpack_pair<T>(w[kk].y);
+                qh[kk][0] = pack_pair<M>(v0.x * inv, v0.y * inv);
+                qh[kk][1] = pack_pair<M>(v1.x * inv, v1.y * inv);
+            }
+            // the scales of heads 2c and 2c + 1, from lanes 8c (g = 2c) and 8c + 4
+            const int e0 = __shfl_sync(kFull, e, 8 * c), e1 = __shfl_sync(kFull, e, 8 * c + 4);
+            qsc0 = qs * __int_as_float((127 + e0) << 23);
+            qsc1 = qs * __int_as_float((127 + e1) << 23);
         }
         // scores of both tiles: S_s[16 tokens][8 heads], K fragments from the
-        // codes. The high and low q parts go to separate accumulators, and the
-        // k steps of both tiles interleave: four independent mma chains.
-        float sc[2][4], sl[2][4];
+        // codes; the k steps of both tiles interleave: two independent mma chains.
+        float sc[2][4];
 #pragma unroll
         for (int s = 0; s < 2; ++s)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sc[s][i] = sl[s][i] = 0.f;
+            for (int i = 0; i < 4; ++i) sc[s][i] = 0.f;
 #pragma unroll
         for (int j = 0; j < C::kJ; ++j) {
             uint32_t xa[2][4], xb[2][4];
@@ -293,23 +308,18 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
                     const uint32_t af[4] = {e4m3x2_to_f16x2(xa[s][t]), e4m3x2_to_f16x2(xb[s][t]),
                                             e4m3x2_to_f16x2(xa[s][t] >> 16), e4m3x2_to_f16x2(xb[s][t] >> 16)};
                     mma_16816<M>(sc[s], af, qh[kk][0], qh[kk][1]);
-                    mma_16816<M>(sl[s], af, ql[kk][0], ql[kk][1]);
                 }
             }
         }
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) sc[s][i] += sl[s][i];
         // softmax over the 32 tokens; x[s][i]: tile s, token g (i = 0, 1) or
         // g + 8 (i = 2, 3), head 2c (i even) or 2c + 1 (i odd)
         float x[2][4];
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            x[s][0] = g < rows[s] ? sc[s][0] : kNegInf;
-            x[s][1] = g < rows[s] ? sc[s][1] : kNegInf;
-            x[s][2] = g + 8 < rows[s] ? sc[s][2] : kNegInf;
-            x[s][3] = g + 8 < rows[s] ? sc[s][3] : kNegInf;
+            x[s][0] = g < rows[s] ? sc[s][0] * qsc0 : kNegInf;
+            x[s][1] = g < rows[s] ? sc[s][1] * qsc1 : kNegInf;
+            x[s][2] = g + 8 < rows[s] ? sc[s][2] * qsc0 : kNegInf;
+            x[s][3] = g + 8 < rows[s] ? sc[s][3] * qsc1 : kNegInf;
         }
         const float c0l = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
         const float c1l = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
