@@ -152,3 +152,29 @@ def test_tcgen05_wait_timeout_sets_the_flag_and_returns():
     o, lse = dev.decode()
     compare(o, lse, *dev.oracle_decode(), "bf16", "tcgen05 after timeout")
     assert pd.pd_read_device_flags(dev.ws) == 0
+
+
+def test_tcgen05_workspace_sizes_follow_the_selection():
+    """The two E4M3 kernels partition the work differently, so their workspace
+    sizes differ; a workspace sized for one and too small for the other is
+    rejected with an error, never written past its end."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("tc_ws", "bf16", [100, 2000, 37, 512], 32, 8, 128, 16, seed=761)
+    ws_tc = pd.pd_paged_decode_fp8_workspace_bytes(w.batch, 32, 8, 128, pd.PD_BF16)
+    pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TENSOR_CORES)
+    ws_mma = pd.pd_paged_decode_fp8_workspace_bytes(w.batch, 32, 8, 128, pd.PD_BF16)
+    assert ws_tc > 0 and ws_mma > 0 and ws_tc != ws_mma
+    dev = Fp8Device(w)  # sized for the mma.sync kernel
+    small, large = (dev.ws, None) if ws_mma < ws_tc else (None, dev.ws)
+    pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TCGEN05)
+    if small is not None:
+        with pytest.raises(pd.PagedecodeError):
+            dev.decode()
+    else:
+        o, lse = dev.decode()  # a larger workspace than needed is fine
+        compare(o, lse, *dev.oracle_decode(), "bf16", "tcgen05 with the mma.sync workspace")
+        assert pd.pd_read_device_flags(large) == 0
+    torch.cuda.synchronize()
