@@ -25,7 +25,7 @@
 //    (row g) and 64q + 32 + 4g + u (row g + 8), so that a lane reads 4
 //    contiguous codes per token row and pairs the tokens' bytes with byte
 //    permutes; o is written back through the same map. No shared-memory
-//    tile is written, which leaves room for a third pipeline stage;
+//    tile is written: a stage holds only the copied codes;
 //  - keeps q in f16 as q 2^-e, e a power of two per head that puts its
 //    largest |q| into [2^14, 2^15): a bf16 or f16 q is then exact in f16 (an
 //    element more than 2^28 below the largest keeps an error under 2^-24 of
@@ -48,9 +48,10 @@ namespace pd {
 
 template <int D>
 struct CfgF8 {
-    // Two stages and up to 12 warps per block at head_dim 128: the step's
-    // instruction stream is latency-bound, so warps (not stages) are what
-    // hides it; 12 warps x 2 stages keep more bytes in flight than 7 x 3.
+    // Two stages of two pages and up to 12 warps per block at head_dim 128
+    // (registers and shared memory both stop there): measured faster than
+    // 3 such stages x 8 warps, and than 3 one-page stages x 16 warps, whose
+    // extra warps do not pay for twice the per-stage work per byte.
     // At 256 the registers of 12 warps would not hold the accumulators: 8.
     static constexpr int kStages = 2;
     static constexpr int kMaxWarps = D <= 128 ? 12 : 8;
