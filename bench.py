@@ -15,10 +15,11 @@ runnable reference implementation) on a bounded sample of the same workload.
 Under torchrun every rank runs its own replica on its own GPU (the decode has
 no exchange step); rank 0 prints.
 
-On one GPU the line also carries `per_config`: the long-context batch (paged
-and contiguous entries), the ragged 70B-shaped batch and the MHA append +
-decode step, each timed the same way in the same process after the headline
-workload (--no-per-config skips them).
+On one GPU the line also carries `per_config`: the long-context batch (paged,
+contiguous and token-major contiguous entries), the ragged 70B-shaped batch,
+the MHA append + decode step and the Llama-shaped batch over an E4M3 pool,
+each timed the same way in the same process after the headline workload
+(--no-per-config skips them).
 """
 from __future__ import annotations
 
@@ -264,9 +265,11 @@ def algorithmic_bytes(w, table=None, mode: str = "paged") -> int:
 # ---------------------------------------------------------------- GPU arm
 
 # Extra workloads timed in the same process after the headline one (one GPU
-# only): the long-context batch through the paged and the contiguous entry,
-# the ragged 70B-shaped batch and the MHA append + decode step.
-PER_CONFIG = ["long_context", "long_context_contiguous", "ragged_70b", "mha_append"]
+# only): the long-context batch through the paged, the contiguous and the
+# token-major contiguous entry, the ragged 70B-shaped batch, the MHA append +
+# decode step, and the Llama-shaped batch over an E4M3 pool.
+PER_CONFIG = ["long_context", "long_context_contiguous", "long_context_nhd", "ragged_70b", "mha_append",
+              "llama3_8b_fp8"]
 # Host lead before the timed steps: the stream first runs a spin kernel of
 # this length, so that every timed step is already queued when the GPU
 # reaches it and no host pause (GC, a thread switch) lands inside a step.
