@@ -100,3 +100,43 @@ def test_fp8_cuda_core_kernel_with_share_tails():
         assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse, l1)
     assert dev.ws[64:72].view(torch.int32).cpu().tolist() == [0, 0]
     compare(o1, l1, *dev.oracle_decode(), w.dtype, "fp8 CUDA-core decode with share tails")
+
+
+@pytest.mark.parametrize("dtype,Hq,Hk", [("bf16", 32, 8), ("f16", 16, 8)])
+def test_fp8_batch_above_staged_table(dtype, Hq, Hk):
+    """600 requests: indptr and last_page_len are read from global memory, not
+    staged in shared memory; group 4 runs the E4M3 tensor-core kernel, group 2
+    the CUDA-core variant."""
+    import paged_kv_gqa_13_gb300 as pd
+
+    code = {"f16": pd.PD_F16, "bf16": pd.PD_BF16}[dtype]
+    want = pd.PD_KERNEL_FP8_TENSOR_CORES if Hq // Hk >= 4 else pd.PD_KERNEL_CUDA_CORES
+    assert pd.pd_decode_kernel_kind(Hq, Hk, 128, code, True) == want
+    rng = np.random.default_rng(341)
+    lens = rng.integers(0, 70, size=600)
+    w = wl.make_paged("fp8_big_batch", dtype, lens, Hq, Hk, 128, 16, seed=342)
+    dev = Fp8Device(w)
+    o, lse = dev.decode()
+    compare(o, lse, *dev.oracle_decode(), dtype, "fp8 batch 600")
+    assert pd.pd_read_device_flags(dev.ws) == 0
+
+
+@pytest.mark.parametrize("lead,trail", [(0, 37), (45, 0), (29, 64)])
+def test_fp8_indices_entries_that_no_request_lists(lead, trail):
+    """`indices` may hold entries outside [indptr[0], indptr[batch]): the E4M3
+    tensor-core kernel's walk skips those positions and still meets every
+    listed page once."""
+    import dataclasses
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("fp8_unlisted", "bf16", [2400, 2390, 2401, 2397], 32, 8, 128, 16, seed=343)
+    t = w.table
+    filler = t.indices[:max(lead, trail)]  # valid page ids that no request lists here
+    t2 = dataclasses.replace(t, indices=np.concatenate([filler[:lead], t.indices, filler[:trail]]).astype(np.int32),
+                             indptr=(t.indptr + lead).astype(np.int32))
+    dev = Fp8Device(w)
+    dev.set_table(t2)
+    o, lse = dev.decode()
+    assert pd.pd_read_device_flags(dev.ws) == 0
+    compare(o, lse, *dev.oracle_decode(), "bf16", f"fp8, {lead} leading, {trail} trailing unlisted entries")
