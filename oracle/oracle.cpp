@@ -100,7 +100,7 @@ double e4m3_value(uint8_t c) {
     const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
     if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
     const int bias = ORACLE_MUTANT == 12 ? 8 : 7;
-    const double v = e == 0 ? std::ldexp(m / 8.0, 1 - bias) : std::ldexp(1.0 + m / 8.0, e - bias);
+    const double v = e == 0 && ORACLE_MUTANT != 14 ? std::ldexp(m / 8.0, 1 - bias) : std::ldexp(1.0 + m / 8.0, e - bias);
     return s ? -v : v;
 }
 
@@ -113,11 +113,12 @@ uint8_t e4m3_round(float x) {
     const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
     const double a = std::fabs(double(x));
     if (std::isinf(a)) return sign | 0x7E;
+    if (ORACLE_MUTANT == 16 && a > 464.0) return sign | 0x7F;  // mutant 16: overflow to NaN
     int best = 0;
     double best_err = a;
     for (int c = 1; c <= 0x7E; ++c) {
         const double err = std::fabs(e4m3_value(uint8_t(c)) - a);
-        if (err < best_err || (err == best_err && (c & 1) == 0)) best = c, best_err = err;
+        if (err < best_err || (err == best_err && (ORACLE_MUTANT == 15 || (c & 1) == 0))) best = c, best_err = err;
     }
     return uint8_t(sign | best);
 }
@@ -147,7 +148,7 @@ void attend(const View& q, size_t q_off, long n, int D, double scale, KAt k_at, 
             double* o, double* lse) {
     if (n <= 0) {
         for (int d = 0; d < D; ++d) o[d] = 0.0;
-        *lse = -std::numeric_limits<double>::infinity();
+        *lse = ORACLE_MUTANT == 18 ? 0.0 : -std::numeric_limits<double>::infinity();
         return;
     }
     std::vector<double> s(static_cast<size_t>(n));
@@ -307,7 +308,7 @@ int oracle_contiguous_decode(const void* q, const void* k_cache, const void* v_c
         auto addr = [&](long t, int d) {
             return contiguous_row(layout, b, kh, t, num_kv_heads, max_kv_len) * size_t(head_dim) + size_t(d);
         };
-        attend(Q, size_t(bh) * head_dim, valid_kv_len, head_dim, scale,
+        attend(Q, size_t(bh) * head_dim, ORACLE_MUTANT == 19 ? max_kv_len : valid_kv_len, head_dim, scale,
                [&](long t, int d) { return K.at(addr(t, d)); },
                [&](long t, int d) { return V.at(addr(t, d)); },
                o_out + size_t(bh) * head_dim, lse_out + bh);
@@ -366,7 +367,8 @@ int oracle_paged_append_fp8(const void* k_new, const void* v_new, const float* k
             for (int d = 0; d < head_dim; ++d) {
                 const size_t dst = ((size_t(page) * num_kv_heads + h) * page_size + size_t(slot)) * head_dim + d;
                 const size_t src = (size_t(b) * num_kv_heads + h) * head_dim + d;
-                k_codes[dst] = e4m3_round(float(KN.at(src)) / k_scale[h]);
+                k_codes[dst] = e4m3_round(ORACLE_MUTANT == 17 ? float(KN.at(src)) * k_scale[h]
+                                                              : float(KN.at(src)) / k_scale[h]);
                 v_codes[dst] = e4m3_round(float(VN.at(src)) / v_scale[h]);
             }
     }
@@ -415,7 +417,7 @@ int oracle_merge_states(const double* o_parts, const double* lse_parts, int num_
         }
         double S = 0.0;
         for (int c = 0; c < num_parts; ++c) S += std::exp(lse_parts[size_t(c) * rows + r] - M);
-        const double L = M + std::log(S);
+        const double L = ORACLE_MUTANT == 20 ? M : M + std::log(S);
         for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
         for (int c = 0; c < num_parts; ++c) {
             const double w = std::exp(ORACLE_MUTANT == 9 ? L - lse_parts[size_t(c) * rows + r] : lse_parts[size_t(c) * rows + r] - L);

@@ -24,6 +24,13 @@ MUTANTS = {
     11: "NHD cache addressed as HND",
     12: "E4M3 exponent bias 8 instead of 7",
     13: "FP8 V scaled by the K scale",
+    14: "E4M3 exponent field 0 decoded as a normal number",
+    15: "E4M3 rounding ties away from zero instead of to the even code",
+    16: "E4M3 rounding overflows to NaN instead of saturating at 448",
+    17: "FP8 append multiplies by the K scale instead of dividing",
+    18: "empty request gives lse 0 instead of -inf",
+    19: "contiguous decode reads max_kv_len rows instead of valid_kv_len",
+    20: "merge normalises by the largest lse instead of the log-sum-exp",
 }
 
 
