@@ -349,10 +349,13 @@ pd_status pd_workspace_init(void* workspace, size_t workspace_bytes, void* strea
 pd_status pd_read_device_flags(const void* workspace, int32_t* flags, void* stream);
 
 /*
- * Plain device-to-device copy kernel (16-byte vector loads and stores, grid
- * sized to the SM count), used to measure the achievable HBM bandwidth in
- * the same process as the decode. dst and src: device, 16-byte aligned,
- * not overlapping; bytes a multiple of 16.
+ * Plain copy kernel (16-byte vector loads and stores, grid sized to the SM
+ * count), used to measure the achievable HBM bandwidth in the same process as
+ * the decode, and to bring a step's small inputs in from pinned host memory.
+ * dst and src: device memory or pinned host memory (cudaHostAlloc /
+ * cudaMallocHost, which kernels reach at its host address under unified
+ * addressing), 16-byte aligned, not overlapping; bytes a multiple of 16.
+ * Enqueued on stream; the caller keeps both buffers alive until it is done.
  */
 pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, void* stream);
 

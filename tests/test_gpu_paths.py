@@ -103,3 +103,44 @@ def test_outputs_in_pinned_host_memory():
     assert dw.flags() == 0
     assert torch.equal(oh.view(torch.int16), o_dev.cpu().view(torch.int16))
     assert torch.equal(lh, l_dev.cpu())
+
+
+def test_copy_bytes_to_and_from_pinned_host_memory():
+    """pd_copy_bytes between pinned host memory and device memory, both ways,
+    bit for bit, at sizes below, at and above one thread's share of the grid;
+    then a decode whose q and page table came in through it matches the
+    oracle."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    rng = np.random.default_rng(96)
+    for n in (16, 4096, 281_888, 3 << 20):
+        h = torch.from_numpy(rng.integers(0, 256, size=n, dtype=np.uint8)).pin_memory()
+        d = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        pd.pd_copy_bytes(d, h, n)
+        back = torch.zeros(n, dtype=torch.uint8).pin_memory()
+        pd.pd_copy_bytes(back, d, n)
+        torch.cuda.synchronize()
+        assert torch.equal(d.cpu(), h), n
+        assert torch.equal(back, h), n
+    w = wl.llama3_8b_bf16(seed=97, batch=6, lo=1, hi=900)
+    dw = DeviceWorkload(w)
+    t = w.table
+    parts = [np.ascontiguousarray(w.q).view(np.uint8).reshape(-1)] + [
+        np.ascontiguousarray(a.astype(np.int32)).view(np.uint8).reshape(-1) for a in (t.indices, t.indptr, t.last_page_len)]
+    offs, total = [], 0
+    for p in parts:
+        offs.append(total)
+        total += (p.size + 15) // 16 * 16
+    h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for o_, p in zip(offs, parts):
+        h_in[o_:o_ + p.size] = torch.from_numpy(p)
+    d_in = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    pd.pd_copy_bytes(d_in, h_in, total)
+    qd = d_in[offs[0]:offs[0] + parts[0].size].view(dw.q.dtype).view(dw.q.shape)
+    ind, ptr, lpl = (d_in[o_:o_ + p.size].view(torch.int32) for o_, p in zip(offs[1:], parts[1:]))
+    pd.pd_paged_decode(qd, dw.k, dw.v, ind, ptr, lpl, dw.o, dw.lse, w.sm_scale, dw.ws)
+    torch.cuda.synchronize()
+    assert dw.flags() == 0
+    compare(dw.o, dw.lse, *oracle.paged_decode_workload(w), w.dtype, "inputs copied in by pd_copy_bytes")
