@@ -140,3 +140,43 @@ def test_fp8_indices_entries_that_no_request_lists(lead, trail):
     o, lse = dev.decode()
     assert pd.pd_read_device_flags(dev.ws) == 0
     compare(o, lse, *dev.oracle_decode(), "bf16", f"fp8, {lead} leading, {trail} trailing unlisted entries")
+
+
+@pytest.mark.parametrize("tcgen05", [False, True])
+def test_fp8_decode_replays_from_a_cuda_graph(tcgen05):
+    """The E4M3 decode (either tensor-core kernel) captured once into a CUDA
+    graph and replayed: bit-identical to the direct call, and it reads new q
+    and new page contents in place."""
+    import torch
+
+    import paged_kv_gqa_13_gb300 as pd
+
+    w = wl.make_paged("fp8_graph", "bf16", [700, 1, 2400, 33, 1600], 32, 8, 128, 16, seed=344)
+    pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TCGEN05 if tcgen05 else pd.PD_KERNEL_FP8_TENSOR_CORES)
+    try:
+        dev = Fp8Device(w)  # the workspace size follows the selected kernel
+        want = pd.PD_KERNEL_FP8_TCGEN05 if tcgen05 else pd.PD_KERNEL_FP8_TENSOR_CORES
+        assert pd.pd_decode_kernel_kind(32, 8, 128, pd.PD_BF16, True) == want
+        ref_o, ref_lse = (x.clone() for x in dev.decode())  # the first call plans the shape
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            dev.decode()
+        for _ in range(2):
+            dev.o.fill_(7)
+            dev.lse.fill_(7)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(dev.o.view(torch.int16), ref_o.view(torch.int16))
+            assert torch.equal(dev.lse, ref_lse)
+        q2 = wl.normal(w.q.shape, w.dtype, wl.stream_key(w.seed + 5, "q"))
+        dev.q.copy_(to_dev(q2, w.dtype))
+        w.q = q2
+        dev.k8 ^= np.uint8(0x80)  # every K value negated (NaN codes in unused rows stay NaN)
+        dev.k.copy_(torch.from_numpy(dev.k8).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert pd.pd_read_device_flags(dev.ws) == 0
+        compare(dev.o, dev.lse, *dev.oracle_decode(), "bf16", "fp8 graph replay, new q and K codes")
+    finally:
+        pd.pd_select_fp8_kernel(pd.PD_KERNEL_FP8_TENSOR_CORES)
