@@ -17,15 +17,18 @@
 //    the f16 mma sees them exactly). The 16 dims of k step kk = 4j + t that
 //    lane (g, c) holds are not the mma's canonical columns but dims
 //    k_base(c, j) + 4t + {0..3}, k_base = 128 (j >> 1) + 32c + 16 (j & 1):
-//    one 16-byte load per row feeds four k steps, and the 8 lanes of rows g
-//    and g + 1 (one load phase) read 8 different 16-byte pieces. q takes the
-//    same permutation, so the dot products are unchanged;
-//  - builds the V operand of the P.V mma from the codes in the same way: the
-//    accumulator rows of m tile mt = 4q + u stand for dims 64q + 4g + u
-//    (row g) and 64q + 32 + 4g + u (row g + 8), so that a lane reads 4
-//    contiguous codes per token row and pairs the tokens' bytes with byte
-//    permutes; o is written back through the same map. No shared-memory
-//    tile is written: a stage holds only the copied codes;
+//    one 16-byte load per row feeds four k steps, and the 8 lanes of one
+//    load phase read 8 different 16-byte pieces. q takes the same
+//    permutation, so the dot products are unchanged. Score row g of a tile
+//    holds token 2g - (g & 1) and row g + 8 that token + 2 (see below);
+//  - builds the V operand of the P.V mma with the transposing 8-bit
+//    ldmatrix (16 tokens x 16 dims per matrix): it hands lane (g, c) the
+//    codes of tokens 4c .. 4c+3 of dims g and g + 8, which is the A
+//    fragment of m tile "16 dims" once each token pair is widened, with the
+//    mma's k index 2c, 2c+1 standing for tokens 4c, 4c+1 and 2c+8, 2c+9 for
+//    4c+2, 4c+3. The score rows' token order above makes P leave movmatrix
+//    in that same order. No shared-memory tile is written: a stage holds
+//    only the copied codes;
 //  - keeps q in f16 as q 2^-e, e a power of two per head that puts its
 //    largest |q| into [2^14, 2^15): a bf16 or f16 q is then exact in f16 (an
 //    element more than 2^28 below the largest keeps an error under 2^-24 of
@@ -45,6 +48,16 @@
 #include "pd_decode_mma.cuh"
 
 namespace pd {
+
+// Two 16 x 16 byte matrices from shared memory, transposed: lanes 0-15 give
+// the addresses of matrix 0's rows, lanes 16-31 those of matrix 1. Lane
+// 4 g + q receives rows 4q .. 4q+3 of byte column g (r[0]) and of column g + 8
+// (r[1]) of matrix 0, and the same of matrix 1 in r[2], r[3].
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
 
 template <int D>
 struct CfgF8 {
@@ -176,7 +189,11 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
     float qsc0 = 0.f, qsc1 = 0.f;  // 2^e * sm_scale * log2 e * k_scale of heads 2c and 2c + 1
     float acc[kKS][4];  // P.V accumulators: o^T[v_dim(mt, 0 / 1)][head 2c (+1)]
     // The dim that accumulator row g (hi = 0) or g + 8 (hi = 1) of m tile mt stands for.
-    auto v_dim = [&](int mt, int hi) { return 64 * (mt >> 2) + 32 * hi + 4 * g + (mt & 3); };
+    auto v_dim = [&](int mt, int hi) { return 16 * mt + 8 * hi + g; };
+    // Score row g of a tile holds token rg0 and row g + 8 token rg0 + 2, so
+    // that P leaves movmatrix with lane (g, c) holding tokens 4c .. 4c+3: the
+    // order in which ldmatrix hands out the V codes.
+    const int rg0 = 2 * g - (g & 1);
     float m0, m1, l0, l1;
     auto reset_state = [&]() {
 #pragma unroll
@@ -292,11 +309,12 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             uint32_t xa[2][4], xb[2][4];
 #pragma unroll
             for (int s = 0; s < C::kSub; ++s) {
-                // rows g and g + 8 of the box holding this 16-byte piece (2c + (j & 1))
-                const uint8_t* kr = stp + s * C::kTileRaw + (j >> 1) * C::kBoxBytes + g * 128 +
-                                    (((2 * c + (j & 1)) ^ g) << 4);
-                const uint4 wa = *reinterpret_cast<const uint4*>(kr);
-                const uint4 wb = *reinterpret_cast<const uint4*>(kr + 8 * 128);
+                // token rows rg0 and rg0 + 2 of the box holding this 16-byte piece (2c + (j & 1))
+                const uint8_t* kb = stp + s * C::kTileRaw + (j >> 1) * C::kBoxBytes;
+                const int pc = 2 * c + (j & 1);
+                const uint4 wa = *reinterpret_cast<const uint4*>(kb + rg0 * 128 + ((pc ^ (rg0 & 7)) << 4));
+                const uint4 wb =
+                    *reinterpret_cast<const uint4*>(kb + (rg0 + 2) * 128 + ((pc ^ ((rg0 + 2) & 7)) << 4));
                 xa[s][0] = wa.x, xa[s][1] = wa.y, xa[s][2] = wa.z, xa[s][3] = wa.w;
                 xb[s][0] = wb.x, xb[s][1] = wb.y, xb[s][2] = wb.z, xb[s][3] = wb.w;
             }
@@ -317,10 +335,10 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
         float x[2][4];
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            x[s][0] = g < rows[s] ? sc[s][0] * qsc0 : kNegInf;
-            x[s][1] = g < rows[s] ? sc[s][1] * qsc1 : kNegInf;
-            x[s][2] = g + 8 < rows[s] ? sc[s][2] * qsc0 : kNegInf;
-            x[s][3] = g + 8 < rows[s] ? sc[s][3] * qsc1 : kNegInf;
+            x[s][0] = rg0 < rows[s] ? sc[s][0] * qsc0 : kNegInf;
+            x[s][1] = rg0 < rows[s] ? sc[s][1] * qsc1 : kNegInf;
+            x[s][2] = rg0 + 2 < rows[s] ? sc[s][2] * qsc0 : kNegInf;
+            x[s][3] = rg0 + 2 < rows[s] ? sc[s][3] * qsc1 : kNegInf;
         }
         const float c0l = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
         const float c1l = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
@@ -360,48 +378,35 @@ __global__ void __launch_bounds__(CfgF8<D>::kMaxWarps * 32, 1)
             bh[s][0] = movm_trans(pack_pair<M>(p0, p1));
             bh[s][1] = movm_trans(pack_pair<M>(p2, p3));
         }
-        // O^T[head_dim][8 heads] += V_s^T[head_dim][16 tokens] P_s[16 tokens][8 heads]. Lane (g, c)
-        // holds tokens 2c, 2c+1 (first register pair) and 2c+8, 2c+9 (second)
-        // of the A fragment: it loads, per token and 64-dim group q, the codes
-        // of dims 64q + 4g + {0..3} and 64q + 32 + 4g + {0..3} (zero for rows
-        // past the valid length, whose zero weights must not meet a NaN code)
-        // and pairs the two tokens' bytes u for m tile 4q + u.
+        // O^T[head_dim][8 heads] += V_s^T[head_dim][16 tokens] P_s[16 tokens][8 heads]. m tile mt
+        // holds dims 16 mt .. 16 mt + 15; ldmatrix hands lane (g, c) the codes of tokens
+        // 4c .. 4c+3 of dims g and g + 8, which is the A fragment once the token pairs
+        // are widened (k index 2c, 2c+1 <-> tokens 4c, 4c+1; 2c+8, 2c+9 <-> 4c+2, 4c+3).
+        // Tokens past the valid length are zeroed, so that their zero weights never
+        // meet a NaN code.
+        const int tr = lane & 15;  // the token row whose address this lane gives
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s) {
             if (rows[s] == 0) continue;
-            const uint8_t* vt = stp + C::kVOff + s * C::kTileRaw + 4 * (g & 3);
-            const int t0 = 2 * c;
+            const int rv = rows[s] - 4 * c;
+            const uint32_t vmask = rv >= 4 ? 0xffffffffu : rv <= 0 ? 0u : (0xffffffffu >> (8 * (4 - rv)));
+            const uint32_t vt = wsm_u32 + uint32_t(slot * C::kStageBytes + C::kVOff + s * C::kTileRaw);
 #pragma unroll
-            for (int q = 0; q < C::kJ; ++q) {
-                // dims 64q + 32h + 4g + {0..3}: 16-byte piece 4 (q & 1) + 2h + (g >> 2)
-                // of box q >> 1, at piece ^ (token & 7) in shared memory
-                const uint8_t* vb = vt + (q >> 1) * C::kBoxBytes;
-                uint32_t w[4][2];
+            for (int mp = 0; mp < kKS / 2; ++mp) {
+                const int mt0 = 2 * mp + (lane >> 4);  // the m tile of this lane's row address
+                const uint32_t addr =
+                    vt + uint32_t((mt0 >> 3) * C::kBoxBytes + tr * 128 + (((mt0 & 7) ^ (tr & 7)) << 4));
+                uint32_t r[4];
+                ldsm_b8_x2_trans(addr, r);
+                if (rows[s] < kMmaRows) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tk = t0 + (i & 1) + 8 * (i >> 1);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int piece = (4 * (q & 1) + 2 * h + (g >> 2)) ^ (tk & 7);
-                        w[i][h] = tk < rows[s] ? *reinterpret_cast<const uint32_t*>(vb + tk * 128 + (piece << 4)) : 0u;
-                    }
+                    for (int i = 0; i < 4; ++i) r[i] &= vmask;
                 }
-                // pr[pair][h][half]: bytes u of tokens (t0, t0+1) (pair 0) or
-                // (t0+8, t0+9) (pair 1), u = 2 * half + (0 | 1 in the 16-bit halves)
-                uint32_t pr[2][2][2];
 #pragma unroll
-                for (int pi = 0; pi < 2; ++pi)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        pr[pi][h][0] = __byte_perm(w[2 * pi][h], w[2 * pi + 1][h], 0x5140);
-                        pr[pi][h][1] = __byte_perm(w[2 * pi][h], w[2 * pi + 1][h], 0x7362);
-                    }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int mt = 4 * q + u, sh = 16 * (u & 1);
-                    const uint32_t af[4] = {e4m3x2_to_f16x2(pr[0][0][u >> 1] >> sh), e4m3x2_to_f16x2(pr[0][1][u >> 1] >> sh),
-                                            e4m3x2_to_f16x2(pr[1][0][u >> 1] >> sh), e4m3x2_to_f16x2(pr[1][1][u >> 1] >> sh)};
-                    mma_16816<M>(acc[mt], af, bh[s][0], bh[s][1]);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
+                                            e4m3x2_to_f16x2(r[2 * h] >> 16), e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+                    mma_16816<M>(acc[2 * mp + h], af, bh[s][0], bh[s][1]);
                 }
             }
         }
